@@ -1,0 +1,423 @@
+"""Benchmark of split-KV decode attention on GB300.
+
+Default workload (N=1): long-context GQA decode -- batch 1, 32 query heads over
+8 KV heads, head_dim 128, 128000 cached tokens, fp16 cache -- over 32 layers
+with distinct caches (32 x 524 MB, far larger than L2).  One step is one
+decode step through the 32 layers: 32 fd_decode calls (split + combine each)
+on one stream.
+
+Printed (one JSON line on rank 0):
+  value        KV-read GB/s: K+V bytes of the 32 layers / device time of a step
+  us_per_layer device time of one layer's fd_decode
+  roofline     fd_split (the dominant kernel): algorithmic bytes per launch /
+               its CUDA-event duration, against the measured HBM copy peak
+  e2e          the same metric through the public API from pinned host
+               buffers: per step, q/K/V/seqlens of one layer copied in, one
+               fd_decode, out/lse copied back
+  cpu_baseline the fp64 oracle on the host cores on a bounded sample
+  clocks       SM clocks and throttle reasons sampled during the timed region
+
+--impl reference times the oracle (the only reference this method has) on
+the same workload, a bounded sample per step.
+
+Multi-GPU: the op has no exchange step, so N GPUs run N independent replicas
+(weak scaling); value sums the bytes of all ranks over the max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "long_gqa_128k"
+METRIC = "decode-attention µs/layer and KV-read HBM GB/s (% of GB300 peak) at 128K ctx"
+PEAK_FALLBACK_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
+                time.sleep(0.05)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, s in enumerate(r[2]) if s.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    import torch.distributed as dist
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, ws
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _traffic_from_profile(src_hash: str):
+    """DRAM bytes per fd_split launch from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "fd_split_long_gqa_128k_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("fd_split_cu_sha256") == src_hash:
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for name in ("fd_split.cu", "fd_device.cuh", "fd_internal.h"):
+        with open(os.path.join(ROOT, "split_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+def _oracle_layer_time(q_h, k_h, v_h, seqlens_h, n_kv_heads, min_seconds):
+    """Time the fp64 oracle over whole layers (all rows) on the host cores."""
+    import oracle
+    threads = oracle.hardware_threads()
+    reps, t_total = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode(q_h, k_h, v_h, seqlens_h, dtype="f16", n_kv_heads=n_kv_heads, n_threads=threads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        if t_total >= min_seconds or reps >= 50:
+            break
+    return t_total / reps, threads, reps
+
+
+def _cpu_inputs(c, seed_layer=0):
+    import numpy as np
+
+    import fd_inputs
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"] + 7919 * seed_layer)
+    k = fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 10 + 7919 * seed_layer)
+    v = fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 11 + 7919 * seed_layer)
+    return q, k, v, np.full(B, T, dtype=np.int32)
+
+
+def run_reference(args):
+    """The oracle as the reference arm.  Each step evaluates a bounded sample
+    of the workload's query rows (the same rows every step) on the host
+    cores, sized so that warm-up + steps take about a minute; the KV-read rate
+    is scaled by the fraction of the layer's rows evaluated."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import fd_inputs
+    import oracle
+    c = fd_inputs.WORKLOADS[WORKLOAD]
+    q, k, v, sl = _cpu_inputs(c)
+    threads = oracle.hardware_threads()
+    rows_total = c["batch"] * c["n_q_heads"]
+    kv_bytes = c["batch"] * c["n_kv_heads"] * c["ctx"] * c["head_dim"] * 2 * 2
+
+    def run(rows):
+        oracle.decode(q, k, v, sl, dtype=c["dtype"], n_kv_heads=c["n_kv_heads"],
+                      rows=list(range(rows)), n_threads=threads)
+
+    t0 = time.perf_counter()
+    run(min(threads, rows_total))
+    t_batch = time.perf_counter() - t0                 # one row per thread
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = max(1, min(rows_total, int(budget / max(t_batch, 1e-6) * min(threads, rows_total))))
+    for _ in range(args.warmup):
+        run(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = kv_bytes * rows / rows_total / dt / 1e9
+    sample = (f"{rows} of the layer's {rows_total} query rows per step ({c['ctx']} tokens each, fp64), "
+              "KV rate scaled by that fraction")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "us_per_layer": dt * 1e6 * rows_total / rows, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seeded",
+        "config": _config(c, None),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(c, S):
+    return {"workload": WORKLOAD, "batch": c["batch"], "n_q_heads": c["n_q_heads"],
+            "n_kv_heads": c["n_kv_heads"], "head_dim": c["head_dim"], "ctx": c["ctx"],
+            "layers": c["layers"], "kv_dtype": c["dtype"], "n_splits": S,
+            "l2": "inputs larger than L2: 32 distinct 524 MB layer caches per step",
+            "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import fd_inputs
+    import split_kv_gb300 as fd
+    from split_kv_gb300 import _build
+
+    rank, local, ws = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    c = fd_inputs.WORKLOADS[WORKLOAD]
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    n_layers = args.layers or c["layers"]
+    sl_h = np.full(B, T, dtype=np.int32)
+    S = fd.fd_plan(B, Hq, Hkv, D, sl_h)
+    fd.check(S, "fd_plan")
+
+    # inputs resident in HBM: distinct q and K/V per layer
+    seqlens = torch.from_numpy(sl_h).to(dev)
+    qs, ks, vs = [], [], []
+    for i in range(n_layers):
+        qs.append(fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"] + 7919 * i, device=dev))
+        ks.append(fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 10 + 7919 * i, device=dev))
+        vs.append(fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 11 + 7919 * i, device=dev))
+    desc = fd.make_desc(qs[0], ks[0], vs[0], max_seqlen=T, n_splits=S)
+    wsb = fd.fd_workspace_size(desc, S)
+    workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    out = torch.empty(n_layers, B, Hq, D, dtype=torch.float32, device=dev)
+    lse = torch.empty(n_layers, B, Hq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step():
+        for i in range(n_layers):
+            rc = fd.fd_decode(desc, qs[i], ks[i], vs[i], seqlens, None, out[i], lse[i], workspace,
+                              wsb, stream=sp)
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    fd.check(fd.fd_device_status(stream), "device status after warm-up")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = _max_over_ranks(ms_local, ws)
+    fd.check(fd.fd_device_status(stream), "device status after timing")
+
+    kv_bytes_layer = B * Hkv * T * D * 2 * 2
+    value = ws * n_layers * kv_bytes_layer / (ms * 1e-3) / 1e9
+    us_layer = ms * 1e3 / n_layers
+
+    # ---- roofline of fd_split: per-launch CUDA events around the kernel alone
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_layers)]
+    split_ms, combine_ms = [], []
+    ec = [torch.cuda.Event(enable_timing=True) for _ in range(n_layers)]
+    for rep in range(max(3, min(20, args.steps // 10))):
+        for i in range(n_layers):
+            ev[i][0].record(stream)
+            fd.check(fd.fd_split_states(desc, qs[i], ks[i], vs[i], seqlens, None, workspace, wsb, stream=sp))
+            ev[i][1].record(stream)
+            fd.check(fd.fd_combine_states(desc, workspace, out[i], lse[i], wsb, stream=sp))
+            ec[i].record(stream)
+        torch.cuda.synchronize()
+        if rep == 0:
+            continue   # warm-up pass
+        for i in range(n_layers):
+            split_ms.append(ev[i][0].elapsed_time(ev[i][1]))
+            combine_ms.append(ev[i][1].elapsed_time(ec[i]))
+    split_avg_ms = statistics.mean(split_ms)
+    ws_write = B * Hq * S * (D + 2) * 4
+    split_alg_bytes = kv_bytes_layer + B * Hq * D * 2 + ws_write + 4 * B
+    peak, peak_src = _peaks()
+    achieved = split_alg_bytes / (split_avg_ms * 1e-3) / 1e9
+    traffic = _traffic_from_profile(_kernel_hash())
+    roofline = {"kernel": "fd_split", "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": peak_src, "alg_bytes_per_launch": split_alg_bytes,
+                "launch_us": split_avg_ms * 1e3, "combine_us": statistics.mean(combine_ms) * 1e3}
+
+    # ---- e2e: public API from pinned host buffers, one layer per step
+    e2e = None
+    if rank == 0 or ws > 1:
+        hq = qs[0].cpu().pin_memory()
+        hk = ks[0].cpu().pin_memory()
+        hv = vs[0].cpu().pin_memory()
+        hsl = torch.from_numpy(sl_h).pin_memory()
+        ho = torch.empty(B, Hq, D, dtype=torch.float32).pin_memory()
+        hl = torch.empty(B, Hq, dtype=torch.float32).pin_memory()
+        dq, dk, dv, dsl = torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0]), \
+            torch.empty_like(seqlens)
+        dout, dl = torch.empty(B, Hq, D, dtype=torch.float32, device=dev), \
+            torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            rc = fd.fd_decode(desc, dq, dk, dv, dsl, None, dout, dl, workspace, wsb, stream=sp)
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode")
+            ho.copy_(dout, non_blocking=True)
+            hl.copy_(dl, non_blocking=True)
+
+        n_e2e = max(3, min(20, args.steps // 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / n_e2e
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hsl.numel() * 4
+        d2h = ho.numel() * 4 + hl.numel() * 4
+        e2e = {"value": ws * kv_bytes_layer / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms, "step": "one layer: H2D q/K/V/seqlens, fd_decode, D2H out/lse"}
+
+    # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        q_h, k_h, v_h = qs[0].cpu(), ks[0].cpu(), vs[0].cpu()
+        t_layer, threads, reps = _oracle_layer_time(q_h, k_h, v_h, sl_h, Hkv, min_seconds=10.0)
+        cpu = {"value": kv_bytes_layer / t_layer / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"one layer of the workload (all {B * Hq} query rows, {T} tokens) "
+                         f"x {reps} repetitions, fp64; {t_layer * 1e6:.0f} us/layer"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": us_layer,
+            "frac_of_hbm_peak": value / peak, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic N(0,1), seeded, fp16 cache",
+            "config": _config(c, S), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": 2 * n_layers * args.steps,
+            "workspace_bytes": wsb, "num_sms": fd.fd_num_sms(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -77,3 +77,19 @@ def block_table(seed: int, batch: int, pages_per_seq: int, n_pages: int | None =
     n_pages = n_pages or batch * pages_per_seq
     perm = page_permutation(seed, n_pages)
     return perm[: batch * pages_per_seq].reshape(batch, pages_per_seq).copy()
+
+
+def randn_chunked(shape, dtype: str, seed: int, device="cpu", gain: float = 1.0):
+    """Like randn, but drawn one leading index at a time (seed*1000003 + i), so
+    caches of tens of GB need only one slice of f32 scratch."""
+    import torch
+    out = torch.empty(*shape, dtype=torch_dtype(dtype), device=device)
+    g = torch.Generator(device=device)
+    for i in range(shape[0]):
+        g.manual_seed(int(seed) * 1000003 + i)
+        x = torch.randn(*shape[1:], generator=g, device=device, dtype=torch.float32)
+        if gain != 1.0:
+            x.mul_(gain)
+        out[i].copy_(x)
+        del x
+    return out

@@ -1,0 +1,189 @@
+/* fd.h -- split-KV decode attention (Flash-Decoding) for GB300 / sm_103a.
+ *
+ * One decode step of attention: for every sequence b and query head h, one
+ * query row q[b,h,:] attends over the first seqlens[b] keys/values of its KV
+ * head in a long fp16 / bf16 cache:
+ *
+ *     s_j = q . k_j / sqrt(D),   out = sum_j softmax(s)_j v_j,
+ *     lse = log sum_j exp(s_j)                       (natural log)
+ *
+ * ("Flash-Decoding: Split-KV Attention for Long-Context Decode", §1 and §2).
+ * The KV sequence of each (b, KV head) is cut into n_splits ranges; one CTA
+ * per (split, KV head, b) streams its range with an online softmax and leaves
+ * an unnormalised partial state (u, m, ell) in a caller-owned fp32 workspace;
+ * a second kernel merges the states exactly with the max-subtracted rule
+ * ("Decode 专项 Attention：把长KV拆开算，再正确合并", §04; the Flash-Decoding
+ * page, §2 "Numerically stable form").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Ownership: every pointer is owned by the caller.  The library never
+ *    allocates, frees or synchronises device memory or streams in fd_decode /
+ *    fd_split_states / fd_combine_states.
+ *  - Device pointers: q, k_cache, v_cache, seqlens, block_table, out, lse and
+ *    workspace are device addresses on the current CUDA device.  Host pointers
+ *    are marked "host".
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  Work is enqueued asynchronously; nothing waits for it.
+ *  - Errors: every entry point returns an fd_status (or a negative fd_status
+ *    where it returns a count).  Arguments are validated on the host before
+ *    anything is enqueued; a rejected call enqueues nothing.  A failed kernel
+ *    launch returns FD_ERR_CUDA.  Conditions only the GPU can see (a wait
+ *    that timed out, a length or page index out of range) are recorded in a
+ *    per-device status word read by fd_device_status(); the kernels never trap.
+ *  - Grouped-query attention: n_kv_heads divides n_q_heads, G = n_q_heads /
+ *    n_kv_heads, and query head h reads KV head h / G (consecutive query heads
+ *    share a KV head).  The G query rows of a group are packed into one CTA so
+ *    each K/V tile is read from HBM once per group ("Flash-Decoding ...", §1
+ *    GQA note).
+ *  - Supported shapes: head_dim 128; G in {1, 2, 4, 8}; kv_dtype FD_F16 or
+ *    FD_BF16; 1 <= n_splits <= 128.  Other shapes return FD_ERR_UNSUPPORTED.
+ */
+#ifndef FD_H_
+#define FD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FD_ABI_VERSION 1
+#define FD_MAX_SPLITS 128   /* the split-count heuristic's cap ("Flash-Decoding ...", §6) */
+#define FD_TILE_TOKENS 128  /* split ranges are whole 128-token tiles; the planner's KV block */
+
+typedef enum fd_status {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = -1,      /* null pointer, bad size/stride, inconsistent shape */
+    FD_ERR_UNSUPPORTED = -2,      /* valid but not implemented (head_dim, G, dtype, page size) */
+    FD_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned */
+    FD_ERR_CUDA = -4,             /* a CUDA runtime / launch error */
+    FD_ERR_DEVICE_TIMEOUT = -5,   /* a kernel wait ran past its limit (device status word) */
+    FD_ERR_DEVICE_BOUNDS = -6     /* a seqlen or block-table entry was out of range (device status word) */
+} fd_status;
+
+typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
+
+/* Problem descriptor: plain data, filled by the caller, read (never kept) by
+ * each call.  Strides are in ELEMENTS; the head dimension is always contiguous.
+ *
+ * q        [batch, n_q_heads, head_dim]: q[b,h,d] at q + b*q_stride_b + h*q_stride_h + d.
+ * Contiguous cache (page_size == 0): key j of (b, KV head g) at
+ *          k_cache + b*k_stride_b + g*k_stride_h + j*k_stride_t, j < kv_extent
+ *          (e.g. a dense [batch, n_kv_heads, T_max, head_dim] tensor: kv_extent = T_max).
+ * Paged cache (page_size > 0): a pool of kv_extent pages; key j of (b, g) at
+ *          k_cache + P*k_stride_b + g*k_stride_h + (j % page_size)*k_stride_t,
+ *          P = block_table[b*max_pages_per_seq + j / page_size]
+ *          (a pool laid out [n_pages, n_kv_heads, page_size, head_dim] or
+ *          [n_pages, page_size, n_kv_heads, head_dim]: only the strides differ).
+ *          Splits are logical token ranges resolved through the table
+ *          ("Flash-Decoding ...", §7 paged-KV row).
+ * v_* strides describe v_cache the same way.
+ * Alignment (TMA): cache base addresses 16-byte aligned and every stride a
+ * multiple of 8 elements (16 bytes); q rows 16-byte aligned. */
+typedef struct fd_desc {
+    int32_t batch;              /* B >= 0; B = 0 enqueues nothing */
+    int32_t n_q_heads;          /* Hq >= 1 */
+    int32_t n_kv_heads;         /* Hkv >= 1, divides Hq */
+    int32_t head_dim;           /* D; 128 */
+    int32_t kv_dtype;           /* fd_dtype of q, K and V: FD_F16 or FD_BF16 */
+    int32_t out_dtype;          /* fd_dtype of out: FD_F32, FD_F16 or FD_BF16 */
+    int64_t q_stride_b, q_stride_h;
+    int64_t k_stride_b, k_stride_h, k_stride_t;
+    int64_t v_stride_b, v_stride_h, v_stride_t;
+    int64_t kv_extent;          /* contiguous: tokens per (b, g) row (T_max); paged: pages in the pool */
+    int32_t page_size;          /* 0 = contiguous; else tokens per page, a power of two >= 8 */
+    int32_t max_pages_per_seq;  /* paged: row length (stride) of block_table */
+    int32_t max_seqlen;         /* host-known upper bound of seqlens[]; used when n_splits <= 0 */
+    int32_t n_splits;           /* >= 1: use it; <= 0: plan it with fd_plan's rule from max_seqlen */
+    int32_t flags;              /* must be 0 */
+    int32_t reserved;           /* must be 0 */
+} fd_desc;
+
+/* ABI version of the loaded library (FD_ABI_VERSION at build time). */
+int32_t fd_abi_version(void);
+
+/* Static, human-readable text for a status code; never NULL. */
+const char* fd_status_string(int32_t status);
+
+/* Number of SMs of CUDA device `device` (-1: the current device), or a
+ * negative fd_status. */
+int32_t fd_num_sms(int32_t device);
+
+/* Split-count heuristic, "Flash-Decoding ...", §6 "How many splits?":
+ * no split when work_items >= 0.8*slots; otherwise, over split counts
+ * s = 1 .. min(max_splits, slots, n_kv_blocks) that change the blocks per
+ * split, the wave efficiency e(s) = w/ceil(w), w = work_items*s/slots, is
+ * computed in IEEE double and the smallest s with e(s) >= 0.85 * max e is
+ * returned.  n_kv_blocks = 0 returns 1.  Pure host code (no CUDA call).
+ * Returns s >= 1, or FD_ERR_INVALID_ARG for work_items < 1, slots < 1,
+ * n_kv_blocks < 0 or max_splits < 1. */
+int32_t fd_plan_splits(int64_t work_items, int64_t slots, int64_t n_kv_blocks,
+                       int32_t max_splits);
+
+/* n_splits for one decode step: fd_plan_splits(batch*n_kv_heads, 2*num_sms,
+ * ceil(max_b seqlens_host[b] / 128), 128).  work is KV heads x batch because a
+ * CTA serves a whole GQA group ("Flash-Decoding ...", §1 GQA note); two slots
+ * per SM as in the page's §6 dispatcher.  seqlens_host: host array of `batch`
+ * lengths (>= 0).  num_sms <= 0 queries the current device.  The result
+ * depends only on batch, n_kv_heads, max seqlen and num_sms; n_q_heads and
+ * head_dim are validated only.  Returns s in [1, 128] or a negative fd_status. */
+int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                const int32_t* seqlens_host, int32_t num_sms);
+
+/* Bytes of workspace fd_decode needs for `n_splits` (<= 0: the split count
+ * fd_decode would plan).  Layout (all fp32, each section 256-byte aligned,
+ * row r = b*n_q_heads + h):
+ *     u  [batch*n_q_heads][n_splits][head_dim]   unnormalised partial outputs
+ *     m  [batch*n_q_heads][n_splits]             max score of the split (natural units of s)
+ *     l  [batch*n_q_heads][n_splits]             sum of exp(s - m) over the split
+ * An empty split holds u = 0, m = -inf, l = 0.  Returns 0 for an invalid
+ * descriptor. */
+size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits);
+
+/* The whole decode step: fd_split_states then fd_combine_states on `stream`.
+ *  q, k_cache, v_cache : device, layouts in fd_desc.
+ *  seqlens             : device int32[batch], 0 <= seqlens[b] <= capacity,
+ *                        capacity = kv_extent (contiguous) or
+ *                        max_pages_per_seq*page_size (paged).
+ *  block_table         : device int32[batch*max_pages_per_seq] (paged), else NULL.
+ *  out                 : device [batch, n_q_heads, head_dim], out_dtype, contiguous.
+ *  lse                 : device float[batch*n_q_heads], natural-log LSE of the
+ *                        scaled scores; NULL to skip.  A row with seqlens[b] = 0
+ *                        gets out = 0 and lse = -inf.
+ *  workspace           : device, >= fd_workspace_size(desc, n_splits) bytes,
+ *                        256-byte aligned; contents on entry are ignored.
+ * Asynchronous; CUDA-graph capturable (no allocation, no synchronisation). */
+fd_status fd_decode(const fd_desc* desc, const void* q, const void* k_cache,
+                    const void* v_cache, const int32_t* seqlens, const int32_t* block_table,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* First half of fd_decode: one CTA per (split, KV head, b) writes the partial
+ * states (u, m, l) of every query row of its GQA group into the workspace. */
+fd_status fd_split_states(const fd_desc* desc, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* seqlens,
+                          const int32_t* block_table, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Second half of fd_decode: merges the n_splits states of each row exactly,
+ *   M = max over non-empty splits of m_i,  w_i = exp(m_i - M) (0 if empty),
+ *   L = sum w_i l_i,  out = sum w_i u_i / L,  lse = M + log L,
+ * and writes out / lse (out = 0, lse = -inf when every split is empty).  The
+ * workspace may hold states written by fd_split_states or by the caller in
+ * the documented layout, which makes this the standalone state merge.
+ * desc->n_splits must be >= 1 here. */
+fd_status fd_combine_states(const fd_desc* desc, const void* workspace, size_t workspace_bytes,
+                            void* out, float* lse, void* stream);
+
+/* Reads (and with clear != 0 resets) the current device's status word after
+ * synchronising `stream`.  FD_OK, FD_ERR_DEVICE_TIMEOUT, FD_ERR_DEVICE_BOUNDS
+ * or FD_ERR_CUDA.  The word is sticky across calls until cleared. */
+fd_status fd_device_status(void* stream, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H_ */

@@ -1,0 +1,64 @@
+// fd_internal.h -- parameters shared by the host ABI (fd_api.cu) and the
+// decode kernels (fd_split.cu, fd_combine.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fdk {
+
+constexpr int kHeadDim = 128;     // D
+constexpr int kTile = 128;        // split granularity in tokens (the planner's KV block)
+constexpr int kSub = 64;          // tokens per pipeline stage
+constexpr int kStages = 3;        // pipeline depth (stages in flight per CTA)
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
+constexpr int kHalfBytes = kSub * 128;                // one [kSub tokens x 64 dims] 16-bit box
+constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
+
+// Device status bits (sticky until fd_device_status(clear)).
+constexpr unsigned kStatusTimeoutBit = 1u;   // an mbarrier wait ran past its limit
+constexpr unsigned kStatusSeqlenBit = 2u;    // seqlens[b] < 0 or beyond the cache capacity
+constexpr unsigned kStatusPageBit = 4u;      // block-table entry outside [0, n_pages)
+
+struct SplitParams {
+    const void* q;
+    int64_t q_sb, q_sh;             // elements
+    const int32_t* seqlens;
+    const int32_t* block_table;     // paged only
+    int32_t max_pages;              // block_table row length
+    int32_t page_size;              // 0 = contiguous
+    int32_t page_shift;             // log2(page_size)
+    int32_t capacity;               // tokens a sequence may hold
+    int32_t n_pages;                // paged pool size
+    int32_t n_q_heads;
+    int32_t n_splits;
+    float score_scale_log2;         // log2(e) / sqrt(D)
+    float* ws_u;                    // [rows][n_splits][D]
+    float* ws_m;                    // [rows][n_splits]
+    float* ws_l;                    // [rows][n_splits]
+};
+
+struct CombineParams {
+    const float* ws_u;
+    const float* ws_m;
+    const float* ws_l;
+    void* out;                      // [rows][D], out_dtype
+    float* lse;                     // [rows] or null
+    int32_t rows;
+    int32_t n_splits;
+    int32_t out_dtype;              // 0 f16, 1 bf16, 2 f32
+};
+
+size_t split_smem_bytes();
+
+// Launchers return cudaGetLastError() after the launch.
+cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
+                         int kv_dtype, int group, int batch, int n_kv_heads, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+// Device status word helpers (fd_split.cu owns the symbol).
+cudaError_t read_status(unsigned* value, cudaStream_t stream, bool clear);
+
+}  // namespace fdk

@@ -1,0 +1,488 @@
+// fd_split.cu -- the split kernel of split-KV decode attention on sm_103a.
+//
+// One CTA per (KV split, KV head, sequence).  It streams the split's K/V
+// rows once, for all G query heads of the KV head's group, and leaves the
+// group's unnormalised partial states (u, m, l) in the workspace:
+//   m = max_j s_j,  l = sum_j exp(s_j - m),  u = sum_j exp(s_j - m) v_j
+// over the split's keys j ("Decode 专项 Attention：把长KV拆开算，再正确合并",
+// §04; the tinyvolt Flash-decoding article's fd_split, which also stores the
+// undivided O with m and l).  Inside the split the online-softmax recurrence
+// of "Flash-Decoding: Split-KV Attention for Long-Context Decode" §4 runs tile
+// by tile; an empty split leaves (u=0, m=-inf, l=0) (same page, §4 bullet on
+// ragged batches).
+//
+// GB300 structure
+//  - Warp 4 is a TMA producer: per 64-token stage it issues four 2-D boxes
+//    [64 tokens x 64 dims] (K low/high half, V low/high half) with 128-byte
+//    swizzle into a 3-stage ring, completing on the stage's "full" mbarrier.
+//    Contiguous caches use one box per half; paged caches one box per page
+//    (page_size >= 8), resolved through the block table a stage ahead.
+//  - Warps 0-3 consume.  Each warp owns 16 of a stage's 64 rows and keeps its
+//    own running (m, l, acc) per query head; the four warp states are merged
+//    exactly at the end of the split (the same max-subtracted rule).
+//    QK: a half-warp covers one 256-byte K row (16 lanes x 8 dims) and the G
+//    partial dot products are reduced with a reduce-scatter butterfly (each
+//    lane ends with one head's score).  PV: each lane owns 4 dims x G heads.
+//  - Scores are kept in base 2: t = (q.k) * log2(e)/sqrt(D), p = 2^(t - m).
+//    The workspace m is converted back to natural units of s.
+//  - Every mbarrier wait is bounded (2 s of wall time); on timeout the kernel
+//    records kStatusTimeout in the device status word, drains its own copies
+//    (bounded) and returns without writing states.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fd_device.cuh"
+#include "fd_internal.h"
+
+namespace fdk {
+
+// Per-device status word: sticky error bits read by fd_device_status().
+__device__ unsigned int g_fd_status = 0;
+
+namespace {
+
+__device__ __forceinline__ void raise_status(unsigned bits) { atomicOr(&g_fd_status, bits); }
+
+// mbar_wait that records a timeout in the status word.
+__device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
+    if (mbar_wait(bar, parity)) return true;
+    raise_status(kStatusTimeoutBit);
+    return false;
+}
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <typename T>
+struct Cvt;
+
+template <>
+struct Cvt<__half> {
+    static __device__ __forceinline__ float2 pair(uint32_t w) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+};
+
+template <>
+struct Cvt<__nv_bfloat16> {
+    // a bf16 pattern is the upper half of the f32 pattern of the same value
+    static __device__ __forceinline__ float2 pair(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void cvt8(const uint4& r, float (&f)[8]) {
+    float2 a = Cvt<T>::pair(r.x), b = Cvt<T>::pair(r.y), c = Cvt<T>::pair(r.z),
+           d = Cvt<T>::pair(r.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <typename T>
+__device__ __forceinline__ void cvt4(const uint2& r, float (&f)[4]) {
+    float2 a = Cvt<T>::pair(r.x), b = Cvt<T>::pair(r.y);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+// One reduce-scatter level over lanes `lane ^ MASK`: of N values per lane,
+// the lane keeps the lower half (MASK bit clear) or the upper half (set),
+// summed with the partner's copy of the same half.
+template <int N, int MASK>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+    const bool up = (lane & MASK) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[i + N / 2];
+        const float keep = up ? v[i + N / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(kFull, send, MASK);
+    }
+}
+
+template <int G>
+struct GroupShape {
+    static constexpr int kLog = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    // lanes whose all-reduced bits are zero own one (row, head) result
+    static constexpr int kOwnerMask = (16 >> kLog) - 1;
+};
+
+// Sums G per-lane partial dot products over the 16 lanes of a half-warp.
+// Afterwards lane l holds the full dot product of head head_of_lane<G>(l).
+template <int G>
+__device__ __forceinline__ float reduce16(float (&v)[G], int lane) {
+    constexpr int LG = GroupShape<G>::kLog;
+    if constexpr (LG >= 1) reduce_scatter<G, 8>(v, lane);
+    if constexpr (LG >= 2) reduce_scatter<G / 2, 4>(v, lane);
+    if constexpr (LG >= 3) reduce_scatter<G / 4, 2>(v, lane);
+#pragma unroll
+    for (int mask = 8 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
+    return v[0];
+}
+
+template <int G>
+__device__ __forceinline__ int head_of_lane(int lane) {
+    constexpr int LG = GroupShape<G>::kLog;
+    int g = 0;
+#pragma unroll
+    for (int k = 0; k < LG; ++k)
+        if (lane & (8 >> k)) g += G >> (k + 1);
+    return g;
+}
+
+// Shared-memory map (dynamic, 1024-byte aligned base for the 128B swizzle).
+constexpr int kOffBars = kStages * kStageBytes;                   // full[kStages], empty[kStages]
+constexpr int kOffP = kOffBars + 128;                             // [warps][16 rows][8 heads] f32
+constexpr int kOffAlpha = kOffP + kConsumerWarps * 16 * 8 * 4;    // [warps][8] f32
+constexpr int kOffFlag = kOffAlpha + kConsumerWarps * 8 * 4;      // abort flag
+constexpr int kSmemUsed = kOffFlag + 16;
+// end-of-split merge area (reuses stage memory once every stage is consumed)
+constexpr int kOffWAcc = 0;                                       // [warps][8][128] f32
+constexpr int kOffWM = kConsumerWarps * 8 * kHeadDim * 4;         // [warps][8]
+constexpr int kOffWL = kOffWM + kConsumerWarps * 8 * 4;           // [warps][8]
+static_assert(kOffWL + kConsumerWarps * 8 * 4 <= kOffBars, "merge area must fit in the stages");
+
+}  // namespace
+
+size_t split_smem_bytes() { return static_cast<size_t>(kSmemUsed) + 1024; }
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int split = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_splits;
+
+    // ---- this split's token range: balanced whole tiles of the sequence
+    int L = __ldg(p.seqlens + b);
+    if (L < 0 || L > p.capacity) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0) raise_status(kStatusSeqlenBit);
+        L = L < 0 ? 0 : p.capacity;
+    }
+    const int n_tiles = (L + kTile - 1) / kTile;
+    const int base = n_tiles / S, rem = n_tiles % S;
+    const int t_begin = split * base + (split < rem ? split : rem);
+    const int t_count = base + (split < rem ? 1 : 0);
+    const int tok0 = t_begin * kTile;
+    const int tok1 = min((t_begin + t_count) * kTile, L);
+    const int n_sub = tok1 > tok0 ? (tok1 - tok0 + kSub - 1) / kSub : 0;
+
+    const uint32_t bar0 = smem_u32(smem + kOffBars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);      // any warp gave up
+    volatile int* cons_abort = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);  // a consumer gave up
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *cons_abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ================= producer warp =================
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+        }
+        const uint64_t policy = policy_evict_first();
+        const bool paged = p.page_size != 0;
+        const int rows = paged ? min(kSub, p.page_size) : kSub;   // tokens per box
+        const int nbox = kSub / rows;                              // boxes per half per stage
+        // physical page for box `lane` of sub-tile i (paged); -1 reads zeros
+        auto page_of = [&](int i) -> int {
+            const int t = tok0 + i * kSub + lane * rows;
+            if (lane >= nbox || i >= n_sub || t >= tok1) return -1;
+            const int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages +
+                                 (t >> p.page_shift));
+            if (pg < 0 || pg >= p.n_pages) {
+                raise_status(kStatusPageBit);
+                return -1;
+            }
+            return pg;
+        };
+        int page_next = paged ? page_of(0) : 0;
+        int issued = 0;
+#pragma unroll 1
+        for (int i = 0; i < n_sub; ++i) {
+            const int st = i % kStages;
+            if (i >= kStages) {
+                const bool ok = wait_or_flag(empty_bar(st), ((i / kStages) - 1) & 1);
+                if (!__all_sync(kFull, ok)) *abort_flag = 1;
+            }
+            if (*abort_flag) break;
+            const int page = page_next;
+            const int tok = tok0 + i * kSub;
+            const uint32_t dst = smem_u32(smem + st * kStageBytes);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(st), kStageBytes);
+            __syncwarp();
+            if (!paged) {
+                if (lane == 0) {
+                    tma_load_4d_hint(dst + 0 * kHalfBytes, &tmK, full_bar(st), 0, tok, kvh, b, policy);
+                    tma_load_4d_hint(dst + 1 * kHalfBytes, &tmK, full_bar(st), 64, tok, kvh, b, policy);
+                    tma_load_4d_hint(dst + 2 * kHalfBytes, &tmV, full_bar(st), 0, tok, kvh, b, policy);
+                    tma_load_4d_hint(dst + 3 * kHalfBytes, &tmV, full_bar(st), 64, tok, kvh, b, policy);
+                }
+            } else if (lane < nbox) {
+                const int in_page = (tok + lane * rows) & (p.page_size - 1);
+                const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
+                tma_load_4d_hint(dst + 0 * kHalfBytes + off, &tmK, full_bar(st), 0, in_page, kvh, page, policy);
+                tma_load_4d_hint(dst + 1 * kHalfBytes + off, &tmK, full_bar(st), 64, in_page, kvh, page, policy);
+                tma_load_4d_hint(dst + 2 * kHalfBytes + off, &tmV, full_bar(st), 0, in_page, kvh, page, policy);
+                tma_load_4d_hint(dst + 3 * kHalfBytes + off, &tmV, full_bar(st), 64, in_page, kvh, page, policy);
+            }
+            issued = i + 1;
+            if (paged) page_next = page_of(i + 1);   // block-table read overlaps the next wait
+        }
+        // Drain: the last sub-tile issued into each stage must have landed
+        // before this CTA may exit (a no-op unless a consumer gave up).
+        if (lane == 0) {
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                wait_or_flag(full_bar(i % kStages), (i / kStages) & 1);
+        }
+        return;
+    }
+
+    // ================= consumer warps 0..3 =================
+    const int cw = warp;
+    const int hw = lane >> 4;                   // which of the two rows of a QK step
+    const int c16 = lane & 15;                  // QK: dims 8*c16 .. 8*c16+7
+    const int qk_half = c16 >> 3, qk_chunk = c16 & 7;
+    const int pv_half = lane >> 4;              // PV: dims 4*lane .. 4*lane+3
+    const int pv_chunk = (lane & 15) >> 1, pv_sub = (lane & 1) * 8;
+    const int g_lane = head_of_lane<G>(lane);
+    const bool owner = (lane & GroupShape<G>::kOwnerMask) == 0;   // per half-warp
+
+    float qf[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(b) * p.q_sb +
+                        static_cast<int64_t>(kvh * G + g) * p.q_sh + 8 * c16;
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow));
+        cvt8<T>(raw, qf[g]);
+    }
+
+    float m_run = -INFINITY;   // base-2 running max of this warp's scores for head g_lane
+    float l_run = 0.f;
+    float acc[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[g][j] = 0.f;
+
+    float* pw = reinterpret_cast<float*>(smem + kOffP) + cw * 16 * 8;
+    float* aw = reinterpret_cast<float*>(smem + kOffAlpha) + cw * 8;
+
+#pragma unroll 1
+    for (int i = 0; i < n_sub; ++i) {
+        const int st = i % kStages;
+        bool ok = wait_or_flag(full_bar(st), (i / kStages) & 1);
+        if (!__all_sync(kFull, ok)) {
+            *cons_abort = 1;
+            *abort_flag = 1;
+            break;
+        }
+        const uint8_t* sb = smem + st * kStageBytes;
+        const int nvalid = min(kSub, tok1 - (tok0 + i * kSub));
+
+        // ---- scores of this warp's 16 rows (two rows per step)
+        float sc[8];
+#pragma unroll
+        for (int step = 0; step < 8; ++step) {
+            const int r = cw * 16 + 2 * step + hw;
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                sb + qk_half * kHalfBytes + r * 128 + ((qk_chunk ^ (r & 7)) << 4));
+            float kf[8];
+            cvt8<T>(raw, kf);
+            float part[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float a = qf[g][0] * kf[0];
+#pragma unroll
+                for (int j = 1; j < 8; ++j) a = fmaf(qf[g][j], kf[j], a);
+                part[g] = a;
+            }
+            const float dot = reduce16<G>(part, lane);
+            sc[step] = r < nvalid ? dot * p.score_scale_log2 : -INFINITY;
+        }
+
+        // ---- online softmax for head g_lane over the warp's 16 rows
+        float mx = sc[0];
+#pragma unroll
+        for (int step = 1; step < 8; ++step) mx = fmaxf(mx, sc[step]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;   // never -inf - -inf
+        const float alpha = fast_exp2(m_run - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int step = 0; step < 8; ++step) {
+            const float pv = fast_exp2(sc[step] - m_use);
+            psum += pv;
+            if (owner) pw[(2 * step + hw) * 8 + g_lane] = pv;
+        }
+        psum += __shfl_xor_sync(kFull, psum, 16);
+        l_run = fmaf(alpha, l_run, psum);
+        m_run = m_new;
+        if (owner && hw == 0) aw[g_lane] = alpha;
+        __syncwarp();
+
+        // ---- PV: acc[g][dims] = alpha_g acc + sum_r p[r][g] v[r][dims]
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float a = aw[g];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[g][j] *= a;
+        }
+        const int nrows = min(16, max(0, nvalid - cw * 16));
+        const uint8_t* vb = sb + (2 + pv_half) * kHalfBytes;
+        auto pv_row = [&](int r16) {
+            const int r = cw * 16 + r16;
+            const uint2 raw = *reinterpret_cast<const uint2*>(
+                vb + r * 128 + (((pv_chunk ^ (r & 7)) << 4) | pv_sub));
+            float vf[4];
+            cvt4<T>(raw, vf);
+            float pg[G];
+            const float* pr = pw + r16 * 8;
+            if constexpr (G >= 4) {
+#pragma unroll
+                for (int g = 0; g < G; g += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(pr + g);
+                    pg[g] = t4.x; pg[g + 1] = t4.y; pg[g + 2] = t4.z; pg[g + 3] = t4.w;
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) pg[g] = pr[g];
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[g][j] = fmaf(pg[g], vf[j], acc[g][j]);
+        };
+        if (nrows == 16) {
+#pragma unroll
+            for (int r16 = 0; r16 < 16; ++r16) pv_row(r16);
+        } else {
+#pragma unroll 1
+            for (int r16 = 0; r16 < nrows; ++r16) pv_row(r16);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
+    }
+
+    // ---- merge the four warp states of each head and write the split's state
+    // Only consumers write cons_abort, and only before this barrier, so every
+    // consumer warp takes the same branch below.
+    named_sync(1, kConsumerWarps * 32);
+    if (*cons_abort) return;   // states are not written after a timeout
+    float* wacc = reinterpret_cast<float*>(smem + kOffWAcc);
+    float* wm = reinterpret_cast<float*>(smem + kOffWM);
+    float* wl = reinterpret_cast<float*>(smem + kOffWL);
+    if (owner && hw == 0) {
+        wm[cw * 8 + g_lane] = m_run;
+        wl[cw * 8 + g_lane] = l_run;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        *reinterpret_cast<float4*>(wacc + (cw * 8 + g) * kHeadDim + 4 * lane) =
+            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+    named_sync(1, kConsumerWarps * 32);
+
+    const int d = threadIdx.x;   // 0 .. 127
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * 8 + g]);
+        float u = 0.f, l = 0.f, m_out = -INFINITY;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = wm[w * 8 + g];
+                const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                u = fmaf(e, wacc[(w * 8 + g) * kHeadDim + d], u);
+                l = fmaf(e, wl[w * 8 + g], l);
+            }
+            m_out = M * kLn2;
+        }
+        const int64_t row = static_cast<int64_t>(b) * p.n_q_heads + kvh * G + g;
+        const int64_t idx = row * S + split;
+        p.ws_u[idx * kHeadDim + d] = u;
+        if (d == 0) {
+            p.ws_m[idx] = m_out;
+            p.ws_l[idx] = l;
+        }
+    }
+}
+
+template <typename T, int G>
+static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                  const SplitParams& p, int batch, int n_kv_heads,
+                                  cudaStream_t stream) {
+    auto kern = fd_split_kernel<T, G>;
+    const size_t smem = split_smem_bytes();
+    // one attribute call per (kernel, device): cheap and safe to repeat
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    dim3 grid(p.n_splits, n_kv_heads, batch);
+    kern<<<grid, kThreads, smem, stream>>>(tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
+                         int kv_dtype, int group, int batch, int n_kv_heads, cudaStream_t stream) {
+#define FD_CASE(TT, GG) return launch_split_t<TT, GG>(tmK, tmV, p, batch, n_kv_heads, stream)
+    if (kv_dtype == 0) {
+        switch (group) {
+            case 1: FD_CASE(__half, 1);
+            case 2: FD_CASE(__half, 2);
+            case 4: FD_CASE(__half, 4);
+            case 8: FD_CASE(__half, 8);
+        }
+    } else {
+        switch (group) {
+            case 1: FD_CASE(__nv_bfloat16, 1);
+            case 2: FD_CASE(__nv_bfloat16, 2);
+            case 4: FD_CASE(__nv_bfloat16, 4);
+            case 8: FD_CASE(__nv_bfloat16, 8);
+        }
+    }
+#undef FD_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t read_status(unsigned* value, cudaStream_t stream, bool clear) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_fd_status, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    if (clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_fd_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
+}  // namespace fdk

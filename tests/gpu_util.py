@@ -1,0 +1,125 @@
+"""Helpers for the GPU parity tests: run the C-ABI path with guard canaries
+around every buffer it writes, and compare with the oracle element by element."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import split_kv_gb300 as fd
+
+GUARD = 256          # guard elements (or bytes) on each side of every written buffer
+ATOL, RTOL = 2e-3, 1e-2
+LSE_ATOL = 1e-3
+
+
+class Guarded:
+    """A device buffer with NaN / 0xA5 canaries on both sides."""
+
+    def __init__(self, n: int, dtype, device, fill_float=float("nan"), align: int = 256):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        pad = GUARD + align // esz
+        self.full = torch.empty(n + 2 * pad, dtype=dtype, device=device)
+        if dtype.is_floating_point:
+            self.full.fill_(fill_float)
+        else:
+            self.full.fill_(0xA5)
+        # first aligned element after the guard
+        base = self.full.data_ptr()
+        start = GUARD
+        while (base + start * esz) % align:
+            start += 1
+        self.start, self.n = start, n
+        self.view = self.full[start:start + n]
+        self.before = self.full[:start].clone()
+        self.after = self.full[start + n:].clone()
+
+    def intact(self) -> bool:
+        """Both canaries hold the exact bit patterns they were filled with."""
+        def bits(t):
+            esz = t.element_size()
+            return t.view({4: torch.int32, 2: torch.int16, 1: torch.uint8}[esz])
+        a = self.full[:self.start]
+        b = self.full[self.start + self.n:]
+        return torch.equal(bits(a), bits(self.before)) and torch.equal(bits(b), bits(self.after))
+
+
+def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=None,
+               n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True):
+    """fd_decode through the C ABI; returns (out [B*Hq, D] f64, lse [B*Hq] f64, S)."""
+    dev = q.device
+    B, Hq, D = q.shape
+    seqlens_h = np.asarray(seqlens_h, dtype=np.int32)
+    seqlens = torch.from_numpy(seqlens_h).to(dev)
+    bt = None
+    mp = 0
+    if page_size:
+        bt = torch.from_numpy(np.ascontiguousarray(block_table, dtype=np.int32)).to(dev)
+        mp = block_table.shape[1]
+    desc = fd.make_desc(q, k, v, n_kv_heads=n_kv_heads, page_size=page_size, max_pages_per_seq=mp,
+                        max_seqlen=int(seqlens_h.max()) if B else 0, n_splits=n_splits,
+                        out_dtype=out_dtype)
+    S = n_splits if n_splits > 0 else fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
+    assert S >= 1
+    desc.n_splits = S
+    wsb = fd.fd_workspace_size(desc, S)
+    assert wsb > 0
+    out = Guarded(B * Hq * D, out_dtype, dev)
+    lse = Guarded(B * Hq, torch.float32, dev)
+    ws = Guarded(wsb, torch.uint8, dev)
+    fd.check(fd.fd_decode(desc, q, k, v, seqlens, bt, out.view, lse.view, ws.view, wsb,
+                          stream=stream), "fd_decode")
+    fd.check(fd.fd_device_status(stream), "device status")
+    torch.cuda.synchronize()
+    if check_guards:
+        assert out.intact(), "fd_decode wrote outside out"
+        assert lse.intact(), "fd_decode wrote outside lse"
+        assert ws.intact(), "fd_decode wrote outside its workspace"
+    o = out.view.float().cpu().double().numpy().reshape(B * Hq, D)
+    l = lse.view.cpu().double().numpy()
+    return o, l, S
+
+
+def assert_parity(got_o, got_l, ref_o, ref_l, what=""):
+    assert not np.isnan(got_o).any(), f"{what}: NaN in out"
+    assert not np.isnan(got_l).any(), f"{what}: NaN in lse"
+    err = np.abs(got_o - ref_o)
+    tol = ATOL + RTOL * np.abs(ref_o)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements out of tolerance, max abs err "
+                           f"{err.max():.3e}")
+    fin = np.isfinite(ref_l)
+    assert np.all(np.isneginf(got_l[~fin])), f"{what}: lse of empty rows must be -inf"
+    assert np.all(np.isfinite(got_l[fin])), f"{what}: non-finite lse"
+    if fin.any():
+        le = np.abs(got_l[fin] - ref_l[fin]).max()
+        assert le <= LSE_ATOL, f"{what}: lse err {le:.3e}"
+    return float(err.max()) if err.size else 0.0
+
+
+def oracle_all(q, k, v, seqlens_h, dtype, n_kv_heads, page_size=0, block_table=None, rows=None):
+    return oracle.decode(q.cpu(), k.cpu(), v.cpu(), seqlens_h, dtype=dtype, n_kv_heads=n_kv_heads,
+                         page_size=page_size, block_table=block_table, rows=rows)
+
+
+def oracle_rows_contiguous(q, k, v, seqlens_h, rows, dtype):
+    """Oracle on selected rows of a huge contiguous cache: copies each
+    (b, kv head) slice the rows read once."""
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    rows = [int(r) for r in rows]
+    res = {}
+    groups = {}
+    for r in rows:
+        b, h = divmod(r, Hq)
+        groups.setdefault((b, h // G), []).append(h)
+    for (b, g), heads in groups.items():
+        L = int(seqlens_h[b])
+        kk = k[b:b + 1, g:g + 1, :max(L, 1)].cpu()
+        vv = v[b:b + 1, g:g + 1, :max(L, 1)].cpu()
+        qq = q[b:b + 1, heads].cpu()
+        o, l = oracle.decode(qq, kk, vv, [L], dtype=dtype, n_kv_heads=1)
+        for i, h in enumerate(heads):
+            res[b * Hq + h] = (o[i], l[i])
+    return np.stack([res[r][0] for r in rows]), np.array([res[r][1] for r in rows])

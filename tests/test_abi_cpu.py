@@ -1,0 +1,164 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header
+declares, plans exactly like both statements of the heuristic in the oracle,
+and rejects bad arguments before touching the GPU.  CPU only."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fd():
+    import split_kv_gb300
+    from split_kv_gb300 import _build
+    _build.build()
+    return split_kv_gb300
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "fd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(fd):
+    declared = _header_functions()
+    assert declared, "no functions parsed from include/fd.h"
+    lib = ctypes.CDLL(fd.library_path())
+    for name in declared:
+        assert hasattr(lib, name), f"libfd.so does not export {name}"
+    assert sorted(fd.EXPORTS) == declared
+
+
+def test_abi_version_and_strings(fd):
+    assert fd.fd_abi_version() == 1
+    for code in range(-6, 1):
+        s = fd.fd_status_string(code)
+        assert s and s != "unknown status"
+    assert fd.fd_status_string(99) == "unknown status"
+
+
+def test_desc_struct_size_matches_header(fd):
+    # 6 int32 + 9 int64 + 6 int32 = 24 + 72 + 24 = 120 bytes, 8-byte aligned
+    assert ctypes.sizeof(fd.FdDesc) == 120
+
+
+def test_plan_splits_matches_oracle_table(fd, golden_dir):
+    import json
+    g = json.load(open(os.path.join(golden_dir, "fd_split_table_132sm.json")))
+    for batch, heads, ctx, work, splits, _ in g["rows"]:
+        assert fd.fd_plan_splits(work, g["slots"], -(-ctx // 128)) == splits
+        assert fd.fd_plan(batch, heads, heads, 128, [ctx] * batch, 132) == splits
+
+
+def test_plan_splits_equals_both_oracle_statements(fd):
+    rng = np.random.default_rng(21)
+    for slots in (264, 296, 304):
+        for work in range(1, 260):
+            for nb in (0, 1, 2, 5, 8, 31, 32, 33, 64, 100, 250, 256, 257, 1000, 1024, 2048, 2100):
+                want = oracle.num_splits_ref(work, slots, nb)
+                assert fd.fd_plan_splits(work, slots, nb) == want, (work, slots, nb)
+    for _ in range(4000):
+        w, s, nb, ms = (int(rng.integers(1, 600)), int(rng.integers(1, 500)),
+                        int(rng.integers(0, 4000)), int(rng.integers(1, 200)))
+        assert fd.fd_plan_splits(w, s, nb, ms) == oracle.plan(w, s, nb, ms)
+
+
+def test_plan_for_the_workloads(fd):
+    """Planned split counts of the five workloads at 148 and 152 SMs."""
+    import fd_inputs
+    W = fd_inputs.WORKLOADS
+    for sms in (148, 152):
+        slots = 2 * sms
+        c = W["long_gqa_128k"]
+        got = fd.fd_plan(1, 32, 8, 128, [c["ctx"]], sms)
+        assert got == oracle.num_splits_ref(8, slots, -(-c["ctx"] // 128))
+        L = fd_inputs.varlen_seqlens(W["varlen_b16"]["seed"])
+        assert fd.fd_plan(16, 32, 8, 128, L, sms) == oracle.num_splits_ref(128, slots, -(-int(L.max()) // 128))
+        assert fd.fd_plan(8, 64, 8, 128, [65536] * 8, sms) == oracle.num_splits_ref(64, slots, 512)
+        for b in (1, 4, 16, 64):
+            for ctx in (1024, 8192, 32768, 131072, 262144):
+                assert fd.fd_plan(b, 32, 8, 128, [ctx] * b, sms) == \
+                    oracle.num_splits_ref(8 * b, slots, -(-ctx // 128))
+    assert fd.fd_plan(1, 32, 8, 128, [128000], 148) == 31
+    assert fd.fd_plan(1, 32, 8, 128, [128000], 152) == 33
+
+
+def test_plan_rejects_bad_arguments(fd):
+    assert fd.fd_plan_splits(0, 264, 10) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan_splits(8, 0, 10) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan_splits(8, 264, -1) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan_splits(8, 264, 10, 0) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan(1, 32, 6, 128, [10], 148) == fd.FD_ERR_INVALID_ARG    # 6 does not divide 32
+    assert fd.fd_plan(2, 32, 8, 128, [10, -1], 148) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan(1, 32, 8, 128, [0], 148) == 1                        # empty sequence
+
+
+def _desc(fd, **kw):
+    d = fd.FdDesc()
+    d.batch, d.n_q_heads, d.n_kv_heads, d.head_dim = 1, 32, 8, 128
+    d.kv_dtype, d.out_dtype = fd.FD_F16, fd.FD_F32
+    d.q_stride_b, d.q_stride_h = 32 * 128, 128
+    d.k_stride_b, d.k_stride_h, d.k_stride_t = 8 * 1024 * 128, 1024 * 128, 128
+    d.v_stride_b, d.v_stride_h, d.v_stride_t = 8 * 1024 * 128, 1024 * 128, 128
+    d.kv_extent = 1024
+    d.max_seqlen = 1024
+    d.n_splits = 4
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_workspace_size_layout(fd):
+    d = _desc(fd)
+    rows, S, D = 32, 4, 128
+    def r256(x):
+        return (x + 255) // 256 * 256
+    want = r256(rows * S * D * 4) + 2 * r256(rows * S * 4)
+    assert fd.fd_workspace_size(d, 4) == want
+    assert fd.fd_workspace_size(d, 129) == 0
+    assert fd.fd_workspace_size(_desc(fd, head_dim=64), 4) == 0
+    assert fd.fd_workspace_size(_desc(fd, n_kv_heads=5), 4) == 0
+
+
+def test_decode_rejects_bad_arguments_without_a_gpu(fd):
+    """Every rejection happens on the host, before any CUDA call."""
+    fake = 1 << 20        # a 16-byte-aligned address that is never dereferenced
+    ws = 1 << 21
+    big = 1 << 30
+    call = lambda d, **kw: fd.fd_decode(
+        d, kw.get("q", fake), kw.get("k", fake), kw.get("v", fake), kw.get("sl", fake),
+        kw.get("bt", None), kw.get("out", fake), kw.get("lse", fake), kw.get("ws", ws),
+        kw.get("wsb", big), stream=0)
+    assert call(None if False else _desc(fd, head_dim=64)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, n_q_heads=24)) == fd.FD_ERR_UNSUPPORTED           # G = 3
+    assert call(_desc(fd, n_q_heads=20)) == fd.FD_ERR_INVALID_ARG           # 8 does not divide 20
+    assert call(_desc(fd, kv_dtype=fd.FD_F32)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, kv_dtype=7)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, out_dtype=9)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, n_splits=129)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, k_stride_t=100)) == fd.FD_ERR_INVALID_ARG          # not 16-byte multiple
+    assert call(_desc(fd, flags=1)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, kv_extent=0)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, page_size=12, max_pages_per_seq=4)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, page_size=4, max_pages_per_seq=4), bt=fake) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, page_size=16, max_pages_per_seq=0), bt=fake) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, page_size=16, max_pages_per_seq=64)) == fd.FD_ERR_INVALID_ARG   # no table
+    assert call(_desc(fd), bt=fake) == fd.FD_ERR_INVALID_ARG                # table without paging
+    assert call(_desc(fd), q=None) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd), k=fake + 8) == fd.FD_ERR_INVALID_ARG             # misaligned cache
+    assert call(_desc(fd), out=None) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd), ws=None) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd), ws=ws + 64) == fd.FD_ERR_WORKSPACE               # misaligned workspace
+    assert call(_desc(fd), wsb=1024) == fd.FD_ERR_WORKSPACE                 # too small
+    assert call(_desc(fd, batch=-1)) == fd.FD_ERR_INVALID_ARG
+    # a zero-size batch is valid and enqueues nothing
+    assert call(_desc(fd, batch=0)) == fd.FD_OK
+    assert fd.fd_combine_states(_desc(fd, n_splits=0), ws, fake, fake, workspace_bytes=big,
+                                stream=0) == fd.FD_ERR_INVALID_ARG

@@ -1,0 +1,345 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by
+element: |got - ref| <= 2e-3 + 1e-2 |ref| for out, |dlse| <= 1e-3, -inf exact.
+Every written buffer is surrounded by canaries that must survive."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fd_inputs
+import oracle
+import split_kv_gb300 as fd
+from gpu_util import assert_parity, oracle_all, oracle_rows_contiguous, run_decode
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from split_kv_gb300 import _build as b
+    b.build()
+    torch.cuda.set_device(DEV)
+    fd.fd_device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+
+
+def _cache(B, Hkv, T, D, dtype, seed, gain=1.0):
+    k = fd_inputs.randn_chunked((B, Hkv, T, D), dtype, seed, device=DEV)
+    v = fd_inputs.randn_chunked((B, Hkv, T, D), dtype, seed + 1, device=DEV)
+    return k, v
+
+
+# ---------------------------------------------------------------- tiny MHA
+@pytest.mark.parametrize("n_splits", [0, 1, 3, 7, 128])
+def test_tiny_mha_split_counts(n_splits):
+    c = fd_inputs.WORKLOADS["tiny_mha"]
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"], device=DEV)
+    k, v = _cache(B, Hkv, T, D, c["dtype"], c["seed"] + 10)
+    sl = np.array([T], dtype=np.int32)
+    got_o, got_l, S = run_decode(q, k, v, sl, n_splits=n_splits)
+    ref_o, ref_l = oracle_all(q, k, v, sl, c["dtype"], Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"tiny_mha S={S}")
+    if n_splits == 0:
+        assert S == oracle.num_splits_ref(B * Hkv, 2 * fd.fd_num_sms(), -(-T // 128))
+
+
+# ---------------------------------------------------------------- shapes
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_group_sizes_and_dtypes(dtype, group):
+    B, Hkv, D, T = 2, 4, 128, 1500
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, Hq, D), dtype, 100 + group, device=DEV)
+    k, v = _cache(B, Hkv, T, D, dtype, 200 + group)
+    sl = np.array([1500, 333], dtype=np.int32)
+    for S in (0, 5):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} {dtype} S={S}")
+
+
+def test_ragged_lengths_and_empty_splits():
+    """Lengths at every tile / stage edge, a length-1 and a length-0 sequence,
+    and split counts that leave most splits empty ("Flash-Decoding ..." §8
+    functional checks)."""
+    lens = [0, 1, 2, 63, 64, 65, 127, 128, 129, 191, 255, 256, 257, 300, 1000, 1025]
+    B, Hq, Hkv, D, T = len(lens), 8, 2, 128, 1100
+    q = fd_inputs.randn((B, Hq, D), "f16", 301, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "f16", 302)
+    sl = np.array(lens, dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
+    for S in (0, 1, 2, 3, 8, 9, 128):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"ragged S={S}")
+        # the empty sequence: zero output and LSE = -inf exactly
+        assert np.all(got_o[:Hq] == 0.0) and np.all(np.isneginf(got_l[:Hq]))
+
+
+def test_adversarial_large_scores():
+    """q scaled so that scores reach about +-80 and beyond: the max
+    subtraction must hold in both kernels, no inf or NaN anywhere."""
+    B, Hq, Hkv, D, T = 2, 16, 4, 128, 32768
+    k, v = _cache(B, Hkv, T, D, "f16", 401)
+    sl = np.array([T, 4099], dtype=np.int32)
+    for gain in (18.0, 40.0):
+        q = fd_inputs.randn((B, Hq, D), "f16", 402, device=DEV, gain=gain)
+        s = torch.einsum("bhd,bgtd->bhgt", q.float(), k.float()) / math.sqrt(D)
+        assert s.abs().max().item() > 75.0
+        del s
+        for S in (0, 1, 128):
+            got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+            ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
+            assert_parity(got_o, got_l, ref_o, ref_l, f"gain={gain} S={S}")
+            assert np.all(np.isfinite(got_l))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
+def test_low_precision_outputs(out_dtype):
+    B, Hq, Hkv, D, T = 2, 8, 2, 128, 2000
+    q = fd_inputs.randn((B, Hq, D), "bf16", 501, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "bf16", 502)
+    sl = np.array([2000, 3], dtype=np.int32)
+    got_o, got_l, _ = run_decode(q, k, v, sl, out_dtype=out_dtype)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "bf16", Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"out {out_dtype}")
+
+
+def test_strided_cache_and_query():
+    """Token-major storage [B, T, Hkv, D] seen as a [B, Hkv, T, D] view, and a
+    query that is a slice of a wider tensor."""
+    B, Hq, Hkv, D, T = 2, 16, 4, 128, 900
+    k_bthd = fd_inputs.randn((B, T, Hkv, D), "f16", 601, device=DEV)
+    v_bthd = fd_inputs.randn((B, T, Hkv, D), "f16", 602, device=DEV)
+    k, v = k_bthd.permute(0, 2, 1, 3), v_bthd.permute(0, 2, 1, 3)
+    q_wide = fd_inputs.randn((B, Hq, 2 * D), "f16", 603, device=DEV)
+    q = q_wide[:, :, D:]
+    sl = np.array([900, 77], dtype=np.int32)
+    got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=4)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, "strided")
+
+
+# ---------------------------------------------------------------- paged
+def _paged_problem(B, Hkv, D, ps, lens, dtype, seed, layout="HND", spare=7):
+    max_pages = max(1, -(-max(lens) // ps))
+    n_pages = B * max_pages + spare
+    if layout == "HND":
+        pk = fd_inputs.randn((n_pages, Hkv, ps, D), dtype, seed, device=DEV)
+        pv = fd_inputs.randn((n_pages, Hkv, ps, D), dtype, seed + 1, device=DEV)
+    else:   # [P, page, Hkv, D] storage seen as [P, Hkv, page, D]
+        pk = fd_inputs.randn((n_pages, ps, Hkv, D), dtype, seed, device=DEV).permute(0, 2, 1, 3)
+        pv = fd_inputs.randn((n_pages, ps, Hkv, D), dtype, seed + 1, device=DEV).permute(0, 2, 1, 3)
+    perm = fd_inputs.page_permutation(seed + 2, n_pages)
+    bt = perm[:B * max_pages].reshape(B, max_pages).copy()
+    return pk, pv, bt
+
+
+@pytest.mark.parametrize("ps", [8, 16, 32, 64, 128, 256])
+def test_paged_page_sizes(ps):
+    B, Hkv, G, D = 3, 2, 8, 128
+    Hq = Hkv * G
+    lens = [3000, 17, 1025]
+    pk, pv, bt = _paged_problem(B, Hkv, D, ps, lens, "bf16", 700 + ps)
+    q = fd_inputs.randn((B, Hq, D), "bf16", 701, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "bf16", Hkv, page_size=ps, block_table=bt)
+    for S in (0, 3):
+        got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"paged ps={ps} S={S}")
+
+
+def test_paged_token_major_pool():
+    B, Hkv, G, D, ps = 2, 4, 4, 128, 16
+    lens = [2049, 500]
+    pk, pv, bt = _paged_problem(B, Hkv, D, ps, lens, "f16", 750, layout="NHD")
+    q = fd_inputs.randn((B, Hkv * G, D), "f16", 751, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "f16", Hkv, page_size=ps, block_table=bt)
+    assert_parity(got_o, got_l, ref_o, ref_l, "paged NHD")
+
+
+@pytest.mark.parametrize("ps", [16, 64])
+def test_paged_identity_table_is_bitwise_contiguous(ps):
+    """A pool holding the contiguous cache page by page, read through the
+    identity table, gives the contiguous result bit for bit."""
+    B, Hkv, G, D, T = 2, 4, 4, 128, 4096
+    k, v = _cache(B, Hkv, T, D, "f16", 801)
+    q = fd_inputs.randn((B, Hkv * G, D), "f16", 802, device=DEV)
+    npp = T // ps
+    pk = k.reshape(B, Hkv, npp, ps, D).permute(0, 2, 1, 3, 4).reshape(B * npp, Hkv, ps, D).contiguous()
+    pv = v.reshape(B, Hkv, npp, ps, D).permute(0, 2, 1, 3, 4).reshape(B * npp, Hkv, ps, D).contiguous()
+    bt = np.arange(B * npp, dtype=np.int32).reshape(B, npp)
+    sl = np.array([4096, 2500], dtype=np.int32)
+    o1, l1, _ = run_decode(q, k, v, sl, n_splits=6)
+    o2, l2, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=6)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- determinism, halves
+def test_bitwise_repeatable_and_halves_equal_whole():
+    B, Hq, Hkv, D, T = 2, 32, 8, 128, 6000
+    q = fd_inputs.randn((B, Hq, D), "f16", 901, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "f16", 902)
+    sl = np.array([6000, 4321], dtype=np.int32)
+    o1, l1, S = run_decode(q, k, v, sl)
+    o2, l2, _ = run_decode(q, k, v, sl)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # fd_split_states + fd_combine_states == fd_decode, bit for bit
+    seqlens = torch.from_numpy(sl).to(DEV)
+    desc = fd.make_desc(q, k, v, max_seqlen=6000, n_splits=S)
+    wsb = fd.fd_workspace_size(desc, S)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    fd.check(fd.fd_split_states(desc, q, k, v, seqlens, None, ws))
+    fd.check(fd.fd_combine_states(desc, ws, out, lse))
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().double().numpy().reshape(-1, D), o1)
+    assert np.array_equal(lse.cpu().double().numpy().reshape(-1), l1)
+
+
+def _states_workspace(desc, S, m, l, u):
+    """A workspace in the documented layout filled with caller states."""
+    rows = desc.batch * desc.n_q_heads
+    D = desc.head_dim
+    r256 = lambda x: (x + 255) // 256 * 256
+    off_m = r256(rows * S * D * 4)
+    off_l = off_m + r256(rows * S * 4)
+    wsb = fd.fd_workspace_size(desc, S)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    ws[:rows * S * D * 4].view(torch.float32).copy_(torch.tensor(u, dtype=torch.float32).reshape(-1))
+    ws[off_m:off_m + rows * S * 4].view(torch.float32).copy_(torch.tensor(m, dtype=torch.float32).reshape(-1))
+    ws[off_l:off_l + rows * S * 4].view(torch.float32).copy_(torch.tensor(l, dtype=torch.float32).reshape(-1))
+    return ws, wsb
+
+
+def test_combine_merges_the_pages_worked_states(golden_dir):
+    """fd_combine_states on caller-given states: the 4.9 worked example (A, B)
+    and the merge-trap states; an all-empty row gives 0 / -inf."""
+    g = json.load(open(os.path.join(golden_dir, "dkv_worked_example.json")))
+    t = json.load(open(os.path.join(golden_dir, "fd_merge_trap.json")))
+    D = 128
+    q = torch.zeros(1, 3, D, dtype=torch.float16, device=DEV)
+    k = torch.zeros(1, 1, 8, D, dtype=torch.float16, device=DEV)
+    desc = fd.make_desc(q, k, k, n_kv_heads=1, n_splits=3)
+    S = 3
+    m = np.full((3, S), -np.inf)
+    l = np.zeros((3, S))
+    u = np.zeros((3, S, D))
+    # row 0: states A and B of the worked example, plus an empty split
+    m[0, :2] = [math.log(2), math.log(4)]
+    l[0, :2] = [g["block_A"]["ell"], g["block_B"]["ell"]]
+    u[0, 0, :] = g["block_A"]["u"]
+    u[0, 1, :] = g["block_B"]["u"]
+    # row 1: merge trap, normalised states (lse_i, 1, o_i)
+    m[1, :] = t["lse"]
+    l[1, :] = 1.0
+    u[1, :, :2] = np.array(t["o"])
+    # row 2: every split empty
+    ws, wsb = _states_workspace(desc, S, m, l, u)
+    out = torch.empty(3, D, dtype=torch.float32, device=DEV)
+    lse = torch.empty(3, dtype=torch.float32, device=DEV)
+    fd.check(fd.fd_combine_states(desc, ws, out, lse, wsb))
+    torch.cuda.synchronize()
+    o, L = out.cpu().double().numpy(), lse.cpu().double().numpy()
+    np.testing.assert_allclose(o[0], g["merged"]["output"], rtol=2e-6)
+    assert L[0] == pytest.approx(math.log(10.0), abs=2e-6)
+    np.testing.assert_allclose(o[1, :2], t["printed_stable_merge"], rtol=0, atol=2e-6)
+    assert np.all(o[1, 2:] == 0.0)
+    assert L[1] == pytest.approx(t["printed_merged_lse"], abs=2e-5)
+    assert np.all(o[2] == 0.0) and np.isneginf(L[2])
+
+
+# ---------------------------------------------------------------- device bounds checks
+def test_out_of_range_lengths_and_pages_are_reported():
+    """Lengths beyond the capacity and block-table entries outside the pool are
+    clamped / read as zeros on the device and reported in the status word."""
+    B, Hkv, G, D, ps = 2, 2, 4, 128, 16
+    pk, pv, bt = _paged_problem(B, Hkv, D, ps, [256, 256], "f16", 951)
+    q = fd_inputs.randn((B, Hkv * G, D), "f16", 952, device=DEV)
+    seqlens = torch.tensor([256, 256], dtype=torch.int32, device=DEV)
+    desc = fd.make_desc(q, pk, pv, page_size=ps, max_pages_per_seq=bt.shape[1], n_splits=2)
+    wsb = fd.fd_workspace_size(desc, 2)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty(B, Hkv * G, D, dtype=torch.float32, device=DEV)
+    bad_bt = bt.copy()
+    bad_bt[1, 3] = pk.shape[0] + 5
+    bt_dev = torch.from_numpy(bad_bt).to(DEV)
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    fd.check(fd.fd_decode(desc, q, pk, pv, seqlens, bt_dev, out, None, ws))
+    assert fd.fd_device_status(clear=True) == fd.FD_ERR_DEVICE_BOUNDS
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    too_long = torch.tensor([256, 10_000], dtype=torch.int32, device=DEV)
+    fd.check(fd.fd_decode(desc, q, pk, pv, too_long, torch.from_numpy(bt).to(DEV), out, None, ws))
+    assert fd.fd_device_status(clear=True) == fd.FD_ERR_DEVICE_BOUNDS
+    assert not torch.isnan(out).any()
+
+
+# ---------------------------------------------------------------- the workloads at full size
+def test_varlen_b16_full():
+    c = fd_inputs.WORKLOADS["varlen_b16"]
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    sl = fd_inputs.varlen_seqlens(c["seed"], B, T)
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"], device=DEV)
+    k, v = _cache(B, Hkv, T, D, c["dtype"], c["seed"] + 10)
+    got_o, got_l, S = run_decode(q, k, v, sl)
+    ref_o, ref_l = oracle_all(q, k, v, sl, c["dtype"], Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"varlen S={S}")
+
+
+def test_long_gqa_128k_one_layer():
+    """The headline workload at full size, in the bench's launch configuration
+    (planned split count), every query row against the oracle."""
+    c = fd_inputs.WORKLOADS["long_gqa_128k"]
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"], device=DEV)
+    k, v = _cache(B, Hkv, T, D, c["dtype"], c["seed"] + 10)
+    sl = np.array([T], dtype=np.int32)
+    got_o, got_l, S = run_decode(q, k, v, sl)
+    assert S == fd.fd_plan(1, Hq, Hkv, D, sl)
+    ref_o, ref_l = oracle_all(q, k, v, sl, c["dtype"], Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"long_gqa_128k S={S}")
+
+
+def test_paged_b8_full_sampled_rows():
+    c = fd_inputs.WORKLOADS["paged_b8"]
+    B, Hq, Hkv, D, T, ps = (c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"],
+                            c["page_size"])
+    npp = T // ps
+    n_pages = B * npp
+    pk = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), c["dtype"], c["seed"], device=DEV)
+    pv = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), c["dtype"], c["seed"] + 1, device=DEV)
+    bt = fd_inputs.block_table(c["seed"] + 2, B, npp, n_pages)
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"] + 3, device=DEV)
+    sl = np.full(B, T, dtype=np.int32)
+    got_o, got_l, S = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt)
+    rows = np.random.default_rng(5).choice(B * Hq, size=64, replace=False)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, c["dtype"], Hkv, page_size=ps, block_table=bt, rows=rows)
+    assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"paged_b8 S={S}")
+
+
+@pytest.mark.parametrize("batch", [1, 4, 16, 64])
+def test_sweep_plans_and_sampled_rows(batch):
+    c = fd_inputs.WORKLOADS["sweep"]
+    Hq, Hkv, D = c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
+    rng = np.random.default_rng(batch)
+    for ctx in c["ctxs"]:
+        sl = np.full(batch, ctx, dtype=np.int32)
+        q = fd_inputs.randn((batch, Hq, D), "f16", c["seed"] + batch, device=DEV)
+        k, v = _cache(batch, Hkv, ctx, D, "f16", c["seed"] + 7 * batch + ctx)
+        got_o, got_l, S = run_decode(q, k, v, sl)
+        assert S == oracle.num_splits_ref(batch * Hkv, 2 * fd.fd_num_sms(), -(-ctx // 128))
+        n_rows = batch * Hq if batch * Hq * ctx <= 4 * 32 * 262144 else 16
+        rows = np.sort(rng.choice(batch * Hq, size=min(n_rows, batch * Hq), replace=False))
+        ref_o, ref_l = oracle_rows_contiguous(q, k, v, sl, rows, "f16")
+        assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"sweep B={batch} ctx={ctx} S={S}")
+        del k, v
+        torch.cuda.empty_cache()
