@@ -214,6 +214,7 @@ def _states_workspace(desc, S, m, l, u):
     off_m = r256(rows * S * D * 4)
     off_l = off_m + r256(rows * S * 4)
     wsb = fd.fd_workspace_size(desc, S)
+    assert wsb >= off_l + rows * S * 4
     ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
     ws[:rows * S * D * 4].view(torch.float32).copy_(torch.tensor(u, dtype=torch.float32).reshape(-1))
     ws[off_m:off_m + rows * S * 4].view(torch.float32).copy_(torch.tensor(m, dtype=torch.float32).reshape(-1))
@@ -228,8 +229,8 @@ def test_combine_merges_the_pages_worked_states(golden_dir):
     t = json.load(open(os.path.join(golden_dir, "fd_merge_trap.json")))
     D = 128
     q = torch.zeros(1, 3, D, dtype=torch.float16, device=DEV)
-    k = torch.zeros(1, 1, 8, D, dtype=torch.float16, device=DEV)
-    desc = fd.make_desc(q, k, k, n_kv_heads=1, n_splits=3)
+    k = torch.zeros(1, 3, 8, D, dtype=torch.float16, device=DEV)
+    desc = fd.make_desc(q, k, k, n_kv_heads=3, n_splits=3)
     S = 3
     m = np.full((3, S), -np.inf)
     l = np.zeros((3, S))
