@@ -182,6 +182,40 @@ fd_status fd_combine_states(const fd_desc* desc, const void* workspace, size_t w
  * or FD_ERR_CUDA.  The word is sticky across calls until cleared. */
 fd_status fd_device_status(void* stream, int32_t clear);
 
+/* Size of the fixed device workspace behind fd_decode_static: 8 MiB, enough
+ * for batch*n_q_heads*n_splits up to 16131 query-row splits at head_dim 128
+ * (each needs (head_dim + 2) * 4 bytes). */
+#define FD_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* fd_decode for callers that cannot allocate device memory.  The pages
+ * describe no such entry point; it is an addition of this library.
+ *
+ * Some callers cannot call cudaMalloc or any allocator at the moment they
+ * decode: code running under a custom allocator that must not be re-entered,
+ * embedders that forbid device allocations after start-up, or runtimes that
+ * own every byte of device memory themselves.  For them this entry point
+ * takes the same descriptor, inputs and outputs as fd_decode but no
+ * workspace: the split states live in a fixed FD_STATIC_WORKSPACE_BYTES
+ * array of device memory that the library holds on every GPU that loads it,
+ * until the process exits.
+ *
+ *  - It allocates nothing and frees nothing (no cudaMalloc, cudaFree or other
+ *    allocating routine).  The first call on a device looks up the array's
+ *    device address (cudaGetSymbolAddress) with that device current; make
+ *    that first call before any stream capture on the device.
+ *  - Problems whose workspace (fd_workspace_size) exceeds
+ *    FD_STATIC_WORKSPACE_BYTES are rejected with FD_ERR_WORKSPACE before
+ *    anything is enqueued.
+ *  - Every call on a device shares the one array, and the array keeps what
+ *    the last call left in it.  The split kernel overwrites every state the
+ *    combine reads, so nothing needs clearing between calls, but calls whose
+ *    kernels can overlap on the GPU (other streams, other host threads) race
+ *    on the array: order them, e.g. issue them on one stream.
+ * Arguments, layouts, errors and results are those of fd_decode. */
+fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* seqlens,
+                           const int32_t* block_table, void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,13 +36,14 @@ FD_ERR_DEVICE_BOUNDS = -6
 FD_F16, FD_BF16, FD_F32 = 0, 1, 2
 FD_MAX_SPLITS = 128
 FD_TILE_TOKENS = 128
+FD_STATIC_WORKSPACE_BYTES = 8 << 20
 
 LIB_PATH = _build.LIB_PATH
 
 # every function the header declares (checked against include/fd.h by the tests)
 EXPORTS = ("fd_abi_version", "fd_status_string", "fd_num_sms", "fd_plan_splits", "fd_plan",
            "fd_workspace_size", "fd_decode", "fd_split_states", "fd_combine_states",
-           "fd_device_status")
+           "fd_device_status", "fd_decode_static")
 
 
 class FdDesc(ctypes.Structure):
@@ -103,6 +104,7 @@ def _load():
             "fd_split_states": (i32, [dp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "fd_combine_states": (i32, [dp, vp, sz, vp, vp, vp]),
             "fd_device_status": (i32, [vp, i32]),
+            "fd_decode_static": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -189,6 +191,17 @@ def fd_combine_states(desc: FdDesc, workspace, out, lse, workspace_bytes: int | 
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return int(_load().fd_combine_states(ctypes.byref(desc), _ptr(workspace), int(wb), _ptr(out),
                                          _ptr(lse), _stream(stream)))
+
+
+def fd_decode_static(desc: FdDesc, q, k_cache, v_cache, seqlens, block_table, out, lse,
+                     stream=None) -> int:
+    """fd_decode without a caller workspace: for callers that cannot allocate
+    device memory; the states go to the library's fixed device array
+    (FD_STATIC_WORKSPACE_BYTES per GPU).  Calls that overlap on the GPU race
+    on that array."""
+    return int(_load().fd_decode_static(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(seqlens), _ptr(block_table), _ptr(out), _ptr(lse),
+                                        _stream(stream)))
 
 
 def fd_device_status(stream=None, clear: bool = True) -> int:

@@ -197,6 +197,33 @@ fd_status combine_impl(const fd_desc* d, int32_t S, const void* workspace, size_
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
+// ---- fixed workspace for fd_decode_static (callers that cannot allocate)
+// The split states of fd_decode_static live here instead of in a caller
+// buffer.  Every device that loads the library holds this array until exit.
+static __device__ __align__(256) unsigned char g_static_workspace[FD_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mutex;
+void* g_static_ptr[kMaxStaticDevices] = {};
+
+// Device address of g_static_workspace on the current device, looked up once
+// per device.  (In host code the symbol is only a host-side stand-in; handing
+// it to a kernel would read the wrong memory.)
+fd_status static_workspace(void** ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FD_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxStaticDevices) return FD_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr)
+            return FD_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *ptr = g_static_ptr[dev];
+    return FD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -256,6 +283,26 @@ fd_status fd_decode(const fd_desc* desc, const void* q, const void* k_cache, con
     st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, workspace, workspace_bytes, s);
     if (st != FD_OK) return st;
     return combine_impl(desc, S, workspace, workspace_bytes, out, lse, s);
+}
+
+fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* seqlens, const int32_t* block_table,
+                           void* out, float* lse, void* stream) {
+    fd_status st = check_desc(desc);
+    if (st != FD_OK) return st;
+    if (out == nullptr) return FD_ERR_INVALID_ARG;
+    const int32_t S = splits_for(desc);
+    if (S < 1) return static_cast<fd_status>(S < 0 ? S : FD_ERR_INVALID_ARG);
+    const size_t need = ws_layout(static_cast<int64_t>(desc->batch) * desc->n_q_heads, S).total;
+    if (need > FD_STATIC_WORKSPACE_BYTES) return FD_ERR_WORKSPACE;
+    void* ws = nullptr;
+    st = static_workspace(&ws);
+    if (st != FD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, ws,
+                    FD_STATIC_WORKSPACE_BYTES, s);
+    if (st != FD_OK) return st;
+    return combine_impl(desc, S, ws, FD_STATIC_WORKSPACE_BYTES, out, lse, s);
 }
 
 fd_status fd_device_status(void* stream, int32_t clear) {
