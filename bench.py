@@ -51,6 +51,11 @@ def _args():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
+    ap.add_argument("--workload", default=None,
+                    choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep"],
+                    help="time one workload (one JSON line per problem) instead of the default line")
     return ap.parse_args()
 
 
@@ -274,6 +279,8 @@ def run_gpu(args):
         ks.append(fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 10 + 7919 * i, device=dev))
         vs.append(fd_inputs.randn_chunked((B, Hkv, T, D), c["dtype"], c["seed"] + 11 + 7919 * i, device=dev))
     desc = fd.make_desc(qs[0], ks[0], vs[0], max_seqlen=T, n_splits=S)
+    if args.cuda_cores:
+        desc.flags = fd.FD_FLAG_CUDA_CORES
     wsb = fd.fd_workspace_size(desc, S)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     out = torch.empty(n_layers, B, Hq, D, dtype=torch.float32, device=dev)
@@ -404,6 +411,7 @@ def run_gpu(args):
             "config": _config(c, S), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": 2 * n_layers * args.steps,
             "workspace_bytes": wsb, "num_sms": fd.fd_num_sms(),
+            "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores",
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -411,10 +419,144 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- other workloads
+def _time_calls(fn, n_sets, iters, warmup, stream):
+    import torch
+    for i in range(warmup):
+        fn(i % n_sets)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(iters):
+        fn(i % n_sets)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
+    """Distinct input sets of one workload problem (rotated so that the data
+    touched between two uses of a set exceeds the L2)."""
+    import numpy as np
+    import torch
+
+    import fd_inputs
+    import split_kv_gb300 as fd
+    B = batch or c["batch"]
+    Hq, Hkv, D = c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
+    T = ctx or c["ctx"]
+    dt = c["dtype"]
+    seed = c["seed"]
+    sets = []
+    if name == "varlen_b16":
+        sl_h = fd_inputs.varlen_seqlens(seed, B, T)
+    else:
+        sl_h = np.full(B, T, dtype=np.int32)
+    for j in range(n_sets):
+        q = fd_inputs.randn((B, Hq, D), dt, seed + 100 * j, device=dev)
+        if name == "paged_b8":
+            ps = c["page_size"]
+            npp = T // ps
+            n_pages = B * npp
+            k = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), dt, seed + 100 * j + 1, device=dev)
+            v = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), dt, seed + 100 * j + 2, device=dev)
+            bt = torch.from_numpy(fd_inputs.block_table(seed + 2, B, npp, n_pages)).to(dev)
+            desc = fd.make_desc(q, k, v, page_size=ps, max_pages_per_seq=npp, max_seqlen=int(sl_h.max()))
+        else:
+            k = fd_inputs.randn_chunked((B, Hkv, T, D), dt, seed + 100 * j + 1, device=dev)
+            v = fd_inputs.randn_chunked((B, Hkv, T, D), dt, seed + 100 * j + 2, device=dev)
+            bt = None
+            desc = fd.make_desc(q, k, v, max_seqlen=int(sl_h.max()))
+        sets.append((desc, q, k, v, bt))
+    return sets, sl_h
+
+
+def run_suite(args):
+    """One JSON line per problem of a workload: device time per fd_decode call
+    (inputs rotated across distinct sets larger than the L2), K+V GB/s and the
+    fraction of the measured HBM peak; the sweep also times n_splits = 1."""
+    import math as _m
+
+    import numpy as np
+    import torch
+
+    import fd_inputs
+    import split_kv_gb300 as fd
+    from split_kv_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_src = _peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    name = args.workload
+    c = fd_inputs.WORKLOADS[name]
+    if name == "sweep":
+        probs = [(b, t) for b in c["batches"] for t in c["ctxs"]]
+        base = dict(c, batch=None, ctx=None, dtype=c["dtype"])
+    else:
+        probs = [(None, None)]
+        base = c
+    for batch, ctx in probs:
+        B = batch or c["batch"]
+        T = ctx or c["ctx"]
+        per_set = None
+        est = B * c["n_kv_heads"] * T * c["head_dim"] * 4
+        n_sets = max(1, min(256, _m.ceil(4 * l2 / max(est, 1))))
+        sets, sl_h = _problem_sets(name, base, dev, n_sets, batch, ctx)
+        seqlens = torch.from_numpy(sl_h).to(dev)
+        kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * 2 * 2
+        S_plan = fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
+        results = {}
+        for label, S in (("planned", S_plan), ("unsplit", 1)):
+            if label == "unsplit" and name != "sweep":
+                continue
+            descs = []
+            for (desc, q, k, v, bt) in sets:
+                d = desc.copy()
+                d.n_splits = S
+                if args.cuda_cores:
+                    d.flags = fd.FD_FLAG_CUDA_CORES
+                descs.append(d)
+            wsb = fd.fd_workspace_size(descs[0], S)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            out = torch.empty(B, c["n_q_heads"], c["head_dim"], dtype=torch.float32, device=dev)
+            lse = torch.empty(B, c["n_q_heads"], dtype=torch.float32, device=dev)
+
+            def call(j):
+                _, q, k, v, bt = sets[j]
+                rc = fd.fd_decode(descs[j], q, k, v, seqlens, bt, out, lse, ws, wsb,
+                                  stream=stream.cuda_stream)
+                if rc != 0:
+                    raise fd.FdError(rc, "fd_decode")
+
+            iters = max(20, min(400, int(2e9 / max(kv_bytes, 1))))
+            ms = _time_calls(call, n_sets, iters, max(3, args.warmup), stream)
+            results[label] = (S, ms)
+        fd.check(fd.fd_device_status(stream), "device status")
+        S, ms = results["planned"]
+        line = {"workload": name, "batch": B, "ctx": T, "n_q_heads": c["n_q_heads"],
+                "n_kv_heads": c["n_kv_heads"], "kv_dtype": c["dtype"], "n_splits": S,
+                "us_per_call": ms * 1e3, "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+                "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
+                "input_sets": n_sets, "kv_bytes": kv_bytes,
+                "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores"}
+        if "unsplit" in results:
+            S1, ms1 = results["unsplit"]
+            line["us_per_call_unsplit"] = ms1 * 1e3
+            line["kv_gbs_unsplit"] = kv_bytes / (ms1 * 1e-3) / 1e9
+            line["speedup_vs_unsplit"] = ms1 / ms
+        print(json.dumps(line), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload is not None:
+        run_suite(args)
     else:
         run_gpu(args)
 

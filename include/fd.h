@@ -65,6 +65,13 @@ typedef enum fd_status {
 
 typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
 
+/* fd_desc.flags bits.  By default the split kernel computes the packed
+ * group's QK^T and PV on the tensor cores (warp-level MMA, f32 accumulate).
+ * FD_FLAG_CUDA_CORES computes them as FP32 FMAs on the CUDA cores instead:
+ * same memory pipeline, same results within the stated tolerance; kept for
+ * comparison and profiling. */
+#define FD_FLAG_CUDA_CORES 1
+
 /* Problem descriptor: plain data, filled by the caller, read (never kept) by
  * each call.  Strides are in ELEMENTS; the head dimension is always contiguous.
  *
@@ -97,7 +104,7 @@ typedef struct fd_desc {
     int32_t max_pages_per_seq;  /* paged: row length (stride) of block_table */
     int32_t max_seqlen;         /* host-known upper bound of seqlens[]; used when n_splits <= 0 */
     int32_t n_splits;           /* >= 1: use it; <= 0: plan it with fd_plan's rule from max_seqlen */
-    int32_t flags;              /* must be 0 */
+    int32_t flags;              /* 0, or FD_FLAG_CUDA_CORES */
     int32_t reserved;           /* must be 0 */
 } fd_desc;
 

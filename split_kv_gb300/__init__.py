@@ -37,6 +37,7 @@ FD_F16, FD_BF16, FD_F32 = 0, 1, 2
 FD_MAX_SPLITS = 128
 FD_TILE_TOKENS = 128
 FD_STATIC_WORKSPACE_BYTES = 8 << 20
+FD_FLAG_CUDA_CORES = 1
 
 LIB_PATH = _build.LIB_PATH
 

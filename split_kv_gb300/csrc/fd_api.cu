@@ -41,7 +41,7 @@ bool stride_ok(int64_t s) { return s >= 0 && s % 8 == 0 && s < (int64_t(1) << 38
 // done by the callers, which know which pointers they use.
 fd_status check_desc(const fd_desc* d) {
     if (d == nullptr) return FD_ERR_INVALID_ARG;
-    if (d->flags != 0 || d->reserved != 0) return FD_ERR_INVALID_ARG;
+    if ((d->flags & ~FD_FLAG_CUDA_CORES) != 0 || d->reserved != 0) return FD_ERR_INVALID_ARG;
     if (d->batch < 0 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1)
         return FD_ERR_INVALID_ARG;
     if (d->n_q_heads % d->n_kv_heads != 0) return FD_ERR_INVALID_ARG;
@@ -170,7 +170,8 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
     p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
     const cudaError_t e = fdk::launch_split(tmK, tmV, p, d->kv_dtype, d->n_q_heads / d->n_kv_heads,
-                                            d->batch, d->n_kv_heads, stream);
+                                            (d->flags & FD_FLAG_CUDA_CORES) != 0, d->batch,
+                                            d->n_kv_heads, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 

@@ -54,8 +54,10 @@ struct CombineParams {
 size_t split_smem_bytes();
 
 // Launchers return cudaGetLastError() after the launch.
+// cuda_cores selects the CUDA-core (FP32 FMA) consumer instead of the tensor-core one.
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, int group, int batch, int n_kv_heads, cudaStream_t stream);
+                         int kv_dtype, int group, bool cuda_cores, int batch, int n_kv_heads,
+                         cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Device status word helpers (fd_split.cu owns the symbol).

@@ -147,119 +147,95 @@ static_assert(kOffWL + kConsumerWarps * 8 * 4 <= kOffBars, "merge area must fit 
 
 size_t split_smem_bytes() { return static_cast<size_t>(kSmemUsed) + 1024; }
 
-template <typename T, int G>
-__global__ void __launch_bounds__(kThreads, 2)
-    fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+// Everything a CTA knows about its split, shared by the producer and consumers.
+struct SplitCtx {
+    const SplitParams* p;
+    uint8_t* smem;
+    uint32_t bar0;
+    volatile int* abort_flag;   // any warp gave up
+    volatile int* cons_abort;   // a consumer warp gave up
+    int b, kvh, split;
+    int tok0, tok1, n_sub;
 
-    const int split = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int b = blockIdx.z;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int S = p.n_splits;
+    __device__ __forceinline__ uint32_t full_bar(int s) const { return bar0 + 8u * s; }
+    __device__ __forceinline__ uint32_t empty_bar(int s) const { return bar0 + 8u * (kStages + s); }
+};
 
-    // ---- this split's token range: balanced whole tiles of the sequence
-    int L = __ldg(p.seqlens + b);
-    if (L < 0 || L > p.capacity) {
-        if (threadIdx.x == 0 && split == 0 && kvh == 0) raise_status(kStatusSeqlenBit);
-        L = L < 0 ? 0 : p.capacity;
+// ---------------------------------------------------------------------------
+// Producer warp: streams the split's K/V stages with TMA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tmK,
+                                        const CUtensorMap* tmV, int lane) {
+    const SplitParams& p = *c.p;
+    if (lane == 0) {
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
     }
-    const int n_tiles = (L + kTile - 1) / kTile;
-    const int base = n_tiles / S, rem = n_tiles % S;
-    const int t_begin = split * base + (split < rem ? split : rem);
-    const int t_count = base + (split < rem ? 1 : 0);
-    const int tok0 = t_begin * kTile;
-    const int tok1 = min((t_begin + t_count) * kTile, L);
-    const int n_sub = tok1 > tok0 ? (tok1 - tok0 + kSub - 1) / kSub : 0;
-
-    const uint32_t bar0 = smem_u32(smem + kOffBars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);      // any warp gave up
-    volatile int* cons_abort = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);  // a consumer gave up
-
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kConsumerWarps);
+    const uint64_t policy = policy_evict_first();
+    const bool paged = p.page_size != 0;
+    const int rows = paged ? min(kSub, p.page_size) : kSub;   // tokens per box
+    const int nbox = kSub / rows;                              // boxes per half per stage
+    // physical page of box `lane` of sub-tile i (paged); -1 reads zeros
+    auto page_of = [&](int i) -> int {
+        const int t = c.tok0 + i * kSub + lane * rows;
+        if (lane >= nbox || i >= c.n_sub || t >= c.tok1) return -1;
+        const int pg = __ldg(p.block_table + static_cast<size_t>(c.b) * p.max_pages +
+                             (t >> p.page_shift));
+        if (pg < 0 || pg >= p.n_pages) {
+            raise_status(kStatusPageBit);
+            return -1;
         }
-        *abort_flag = 0;
-        *cons_abort = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ================= producer warp =================
-        if (lane == 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
-        }
-        const uint64_t policy = policy_evict_first();
-        const bool paged = p.page_size != 0;
-        const int rows = paged ? min(kSub, p.page_size) : kSub;   // tokens per box
-        const int nbox = kSub / rows;                              // boxes per half per stage
-        // physical page for box `lane` of sub-tile i (paged); -1 reads zeros
-        auto page_of = [&](int i) -> int {
-            const int t = tok0 + i * kSub + lane * rows;
-            if (lane >= nbox || i >= n_sub || t >= tok1) return -1;
-            const int pg = __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages +
-                                 (t >> p.page_shift));
-            if (pg < 0 || pg >= p.n_pages) {
-                raise_status(kStatusPageBit);
-                return -1;
-            }
-            return pg;
-        };
-        int page_next = paged ? page_of(0) : 0;
-        int issued = 0;
+        return pg;
+    };
+    int page_next = paged ? page_of(0) : 0;
+    int issued = 0;
 #pragma unroll 1
-        for (int i = 0; i < n_sub; ++i) {
-            const int st = i % kStages;
-            if (i >= kStages) {
-                const bool ok = wait_or_flag(empty_bar(st), ((i / kStages) - 1) & 1);
-                if (!__all_sync(kFull, ok)) *abort_flag = 1;
-            }
-            if (*abort_flag) break;
-            const int page = page_next;
-            const int tok = tok0 + i * kSub;
-            const uint32_t dst = smem_u32(smem + st * kStageBytes);
-            if (lane == 0) mbar_arrive_expect_tx(full_bar(st), kStageBytes);
-            __syncwarp();
-            if (!paged) {
-                if (lane == 0) {
-                    tma_load_4d_hint(dst + 0 * kHalfBytes, &tmK, full_bar(st), 0, tok, kvh, b, policy);
-                    tma_load_4d_hint(dst + 1 * kHalfBytes, &tmK, full_bar(st), 64, tok, kvh, b, policy);
-                    tma_load_4d_hint(dst + 2 * kHalfBytes, &tmV, full_bar(st), 0, tok, kvh, b, policy);
-                    tma_load_4d_hint(dst + 3 * kHalfBytes, &tmV, full_bar(st), 64, tok, kvh, b, policy);
-                }
-            } else if (lane < nbox) {
-                const int in_page = (tok + lane * rows) & (p.page_size - 1);
-                const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
-                tma_load_4d_hint(dst + 0 * kHalfBytes + off, &tmK, full_bar(st), 0, in_page, kvh, page, policy);
-                tma_load_4d_hint(dst + 1 * kHalfBytes + off, &tmK, full_bar(st), 64, in_page, kvh, page, policy);
-                tma_load_4d_hint(dst + 2 * kHalfBytes + off, &tmV, full_bar(st), 0, in_page, kvh, page, policy);
-                tma_load_4d_hint(dst + 3 * kHalfBytes + off, &tmV, full_bar(st), 64, in_page, kvh, page, policy);
-            }
-            issued = i + 1;
-            if (paged) page_next = page_of(i + 1);   // block-table read overlaps the next wait
+    for (int i = 0; i < c.n_sub; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages) {
+            const bool ok = wait_or_flag(c.empty_bar(st), ((i / kStages) - 1) & 1);
+            if (!__all_sync(kFull, ok)) *c.abort_flag = 1;
         }
-        // Drain: the last sub-tile issued into each stage must have landed
-        // before this CTA may exit (a no-op unless a consumer gave up).
-        if (lane == 0) {
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                wait_or_flag(full_bar(i % kStages), (i / kStages) & 1);
+        if (*c.abort_flag) break;
+        const int page = page_next;
+        const int tok = c.tok0 + i * kSub;
+        const uint32_t dst = smem_u32(c.smem + st * kStageBytes);
+        const uint32_t bar = c.full_bar(st);
+        if (lane == 0) mbar_arrive_expect_tx(bar, kStageBytes);
+        __syncwarp();
+        if (!paged) {
+            if (lane == 0) {
+                tma_load_4d_hint(dst + 0 * kHalfBytes, tmK, bar, 0, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 1 * kHalfBytes, tmK, bar, 64, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 2 * kHalfBytes, tmV, bar, 0, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 3 * kHalfBytes, tmV, bar, 64, tok, c.kvh, c.b, policy);
+            }
+        } else if (lane < nbox) {
+            const int in_page = (tok + lane * rows) & (p.page_size - 1);
+            const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
+            tma_load_4d_hint(dst + 0 * kHalfBytes + off, tmK, bar, 0, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 1 * kHalfBytes + off, tmK, bar, 64, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 2 * kHalfBytes + off, tmV, bar, 0, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 3 * kHalfBytes + off, tmV, bar, 64, in_page, c.kvh, page, policy);
         }
-        return;
+        issued = i + 1;
+        if (paged) page_next = page_of(i + 1);   // block-table read overlaps the next wait
     }
+    // Drain: the last sub-tile issued into each stage must have landed before
+    // this CTA may exit (a no-op unless a consumer gave up).
+    if (lane == 0) {
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+            wait_or_flag(c.full_bar(i % kStages), (i / kStages) & 1);
+    }
+}
 
-    // ================= consumer warps 0..3 =================
-    const int cw = warp;
+// ---------------------------------------------------------------------------
+// Consumer, CUDA-core path: QK^T and PV as FP32 FMAs.
+// Writes the warp's (m, l, acc) into the merge area; false after a timeout.
+// ---------------------------------------------------------------------------
+template <typename T, int G>
+__device__ __forceinline__ bool consume_simt(const SplitCtx& c, int cw, int lane) {
+    const SplitParams& p = *c.p;
     const int hw = lane >> 4;                   // which of the two rows of a QK step
     const int c16 = lane & 15;                  // QK: dims 8*c16 .. 8*c16+7
     const int qk_half = c16 >> 3, qk_chunk = c16 & 7;
@@ -271,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     float qf[G][8];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(b) * p.q_sb +
-                        static_cast<int64_t>(kvh * G + g) * p.q_sh + 8 * c16;
+        const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(c.b) * p.q_sb +
+                        static_cast<int64_t>(c.kvh * G + g) * p.q_sh + 8 * c16;
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow));
         cvt8<T>(raw, qf[g]);
     }
@@ -285,20 +261,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[g][j] = 0.f;
 
-    float* pw = reinterpret_cast<float*>(smem + kOffP) + cw * 16 * 8;
-    float* aw = reinterpret_cast<float*>(smem + kOffAlpha) + cw * 8;
+    float* pw = reinterpret_cast<float*>(c.smem + kOffP) + cw * 16 * 8;
+    float* aw = reinterpret_cast<float*>(c.smem + kOffAlpha) + cw * 8;
 
 #pragma unroll 1
-    for (int i = 0; i < n_sub; ++i) {
+    for (int i = 0; i < c.n_sub; ++i) {
         const int st = i % kStages;
-        bool ok = wait_or_flag(full_bar(st), (i / kStages) & 1);
+        const bool ok = wait_or_flag(c.full_bar(st), (i / kStages) & 1);
         if (!__all_sync(kFull, ok)) {
-            *cons_abort = 1;
-            *abort_flag = 1;
+            *c.cons_abort = 1;
+            *c.abort_flag = 1;
             break;
         }
-        const uint8_t* sb = smem + st * kStageBytes;
-        const int nvalid = min(kSub, tok1 - (tok0 + i * kSub));
+        const uint8_t* sb = c.smem + st * kStageBytes;
+        const int nvalid = min(kSub, c.tok1 - (c.tok0 + i * kSub));
 
         // ---- scores of this warp's 16 rows (two rows per step)
         float sc[8];
@@ -382,17 +358,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int r16 = 0; r16 < nrows; ++r16) pv_row(r16);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(st));
+        if (lane == 0) mbar_arrive(c.empty_bar(st));
     }
 
-    // ---- merge the four warp states of each head and write the split's state
     // Only consumers write cons_abort, and only before this barrier, so every
     // consumer warp takes the same branch below.
     named_sync(1, kConsumerWarps * 32);
-    if (*cons_abort) return;   // states are not written after a timeout
-    float* wacc = reinterpret_cast<float*>(smem + kOffWAcc);
-    float* wm = reinterpret_cast<float*>(smem + kOffWM);
-    float* wl = reinterpret_cast<float*>(smem + kOffWL);
+    if (*c.cons_abort) return false;   // states are not written after a timeout
+    float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
+    float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
+    float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
     if (owner && hw == 0) {
         wm[cw * 8 + g_lane] = m_run;
         wl[cw * 8 + g_lane] = l_run;
@@ -401,8 +376,334 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int g = 0; g < G; ++g)
         *reinterpret_cast<float4*>(wacc + (cw * 8 + g) * kHeadDim + 4 * lane) =
             make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Consumer, tensor-core path: the packed group's QK^T and PV on warp-level
+// MMAs (m16n8k16, f32 accumulate), "swap-AB" so that 16 tokens are the M
+// rows and the group's <= 8 query heads the N columns:
+//   S^T[16 tok x 8 heads]  = K[16 tok x 128]   . Q^T[128 x 8]     (8 MMAs)
+//   O^T[128 dims x 8 heads] += V^T[128 x 16 tok] . P^T[16 tok x 8]  (8 x 2 MMAs)
+// K and V^T fragments come straight from the swizzled stage with ldmatrix
+// (no conversion instructions); P^T is the transposed S^T accumulator
+// (movmatrix), carried as hi + lo 16-bit parts so that PV keeps ~2^-18
+// relative precision in P even for bf16.
+// Lane (gid = lane/4, tig = lane%4) holds heads 2tig, 2tig+1 of tokens gid,
+// gid+8 in S^T and dims 16mb+gid(+8) of the same two heads in O^T.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Mma;
+
+template <>
+struct Mma<__half> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // (lo, hi) -> one 32-bit register of two 16-bit values; also returns what was kept
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi, float& lo_kept, float& hi_kept) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        const float2 f = __half22float2(h);
+        lo_kept = f.x;
+        hi_kept = f.y;
+        uint32_t r;
+        memcpy(&r, &h, 4);
+        return r;
+    }
+};
+
+template <>
+struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi, float& lo_kept, float& hi_kept) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        uint32_t r;
+        memcpy(&r, &h, 4);
+        lo_kept = __uint_as_float(r << 16);
+        hi_kept = __uint_as_float(r & 0xffff0000u);
+        return r;
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <typename T, int G>
+__device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) {
+    static_assert(G <= 8, "the MMA N dimension holds at most 8 heads");
+    const SplitParams& p = *c.p;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;    // this lane's two heads (>= G: padding)
+    const int r0 = cw * 16;                      // the warp's 16 rows of each stage
+
+    // Q^T as the B operand: b0 = q[gid][16kb + 2tig .. +1], b1 = q[gid][16kb + 8 + 2tig .. +1]
+    uint32_t qb[8][2];
+    {
+        const bool real = gid < G;
+        const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(c.b) * p.q_sb +
+                        static_cast<int64_t>(c.kvh * G + (real ? gid : 0)) * p.q_sh;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            const uint32_t lo = __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kb + 2 * tig));
+            const uint32_t hi = __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kb + 8 + 2 * tig));
+            qb[kb][0] = real ? lo : 0u;
+            qb[kb][1] = real ? hi : 0u;
+        }
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY;   // base-2 running max of heads h0, h1
+    float l0 = 0.f, l1 = 0.f;               // this lane's share of the running sums
+    float acc[8][4];
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
+
+    // ldmatrix row addresses (bytes within a half box, before the stage base)
+    // K (A operand, not transposed): matrix j = lane/8 holds tokens +0/+8 and dims +0/+8
+    const int k_row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int k_csel = lane >> 4;
+    // V^T (A operand via .trans): matrix j holds tokens +0/+8 (j/2) and dims +0/+8 (j%2)
+    const int v_row = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int v_csel = (lane >> 3) & 1;
+
+#pragma unroll 1
+    for (int i = 0; i < c.n_sub; ++i) {
+        const int st = i % kStages;
+        const bool ok = wait_or_flag(c.full_bar(st), (i / kStages) & 1);
+        if (!__all_sync(kFull, ok)) {
+            *c.cons_abort = 1;
+            *c.abort_flag = 1;
+            break;
+        }
+        uint8_t* sb = c.smem + st * kStageBytes;
+        const int nvalid = min(kSub, c.tok1 - (c.tok0 + i * kSub));
+
+        // Rows past the sequence end hold whatever the cache holds there; P is
+        // 0 for them, but 0 * NaN would still poison PV, so zero those V rows.
+        if (nvalid < r0 + 16) {
+            uint8_t* vb = sb + 2 * kHalfBytes;
+#pragma unroll
+            for (int idx = lane; idx < 16 * 16; idx += 32) {
+                const int rr = r0 + (idx >> 4);
+                const int ch = idx & 15;
+                if (rr >= nvalid)
+                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + rr * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();   // ordered before the next TMA write of this stage
+            __syncwarp();
+        }
+
+        // ---- S^T = K . Q^T for the warp's 16 tokens
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kbase = smem_u32(sb);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            const int chunk = 2 * kb + k_csel;                     // 16-byte chunk of the row
+            const uint32_t addr = kbase + (chunk >> 3) * kHalfBytes + k_row * 128 +
+                                  (((chunk & 7) ^ (k_row & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4(a, addr);
+            Mma<T>::run(s, a, qb[kb][0], qb[kb][1]);
+        }
+
+        // ---- online softmax (base 2) for heads h0, h1 over the 16 tokens
+        const bool v0 = r0 + gid < nvalid, v1 = r0 + gid + 8 < nvalid;
+        const float sc = p.score_scale_log2;
+        const float t0 = v0 ? s[0] * sc : -INFINITY;   // token gid,   head h0
+        const float t1 = v0 ? s[1] * sc : -INFINITY;   // token gid,   head h1
+        const float t2 = v1 ? s[2] * sc : -INFINITY;   // token gid+8, head h0
+        const float t3 = v1 ? s[3] * sc : -INFINITY;   // token gid+8, head h1
+        float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+        }
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float u0 = n0 == -INFINITY ? 0.f : n0;   // never -inf - -inf
+        const float u1 = n1 == -INFINITY ? 0.f : n1;
+        const float a0 = fast_exp2(m0 - u0), a1 = fast_exp2(m1 - u1);
+        const float p0 = fast_exp2(t0 - u0), p1 = fast_exp2(t1 - u1);
+        const float p2 = fast_exp2(t2 - u0), p3 = fast_exp2(t3 - u1);
+        l0 = fmaf(a0, l0, p0 + p2);
+        l1 = fmaf(a1, l1, p1 + p3);
+        m0 = n0;
+        m1 = n1;
+        if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+                acc[mb][0] *= a0;
+                acc[mb][1] *= a1;
+                acc[mb][2] *= a0;
+                acc[mb][3] *= a1;
+            }
+        }
+
+        // ---- P^T as B fragments: hi + lo parts, transposed in registers
+        float k0, k1, k2, k3;
+        const uint32_t hi01 = Mma<T>::pack(p0, p1, k0, k1);
+        const uint32_t hi23 = Mma<T>::pack(p2, p3, k2, k3);
+        float d0, d1, d2, d3;
+        const uint32_t lo01 = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
+        const uint32_t lo23 = Mma<T>::pack(p2 - k2, p3 - k3, d2, d3);
+        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+
+        // ---- O^T += V^T . P^T
+        const uint32_t vbase = smem_u32(sb + 2 * kHalfBytes);
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+            const int chunk = 2 * mb + v_csel;
+            const uint32_t addr = vbase + (chunk >> 3) * kHalfBytes + v_row * 128 +
+                                  (((chunk & 7) ^ (v_row & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4_trans(a, addr);
+            Mma<T>::run(acc[mb], a, bh0, bh1);
+            Mma<T>::run(acc[mb], a, bl0, bl1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.empty_bar(st));
+    }
+
+    // lane sums -> head sums over the 8 token rows (lanes with equal tig)
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o);
+        l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+
+    named_sync(1, kConsumerWarps * 32);
+    if (*c.cons_abort) return false;   // states are not written after a timeout
+    float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
+    float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
+    float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
+    if (gid == 0) {
+        if (h0 < G) {
+            wm[cw * 8 + h0] = m0;
+            wl[cw * 8 + h0] = l0;
+        }
+        if (h1 < G) {
+            wm[cw * 8 + h1] = m1;
+            wl[cw * 8 + h1] = l1;
+        }
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+        const int d = 16 * mb + gid;
+        if (h0 < G) {
+            wacc[(cw * 8 + h0) * kHeadDim + d] = acc[mb][0];
+            wacc[(cw * 8 + h0) * kHeadDim + d + 8] = acc[mb][2];
+        }
+        if (h1 < G) {
+            wacc[(cw * 8 + h1) * kHeadDim + d] = acc[mb][1];
+            wacc[(cw * 8 + h1) * kHeadDim + d + 8] = acc[mb][3];
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// The split kernel.  TC selects the tensor-core consumer (default) or the
+// CUDA-core one; both leave the same per-warp states for the final merge.
+// ---------------------------------------------------------------------------
+template <typename T, int G, bool TC>
+__global__ void __launch_bounds__(kThreads, 2)
+    fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    SplitCtx c;
+    c.p = &p;
+    c.smem = smem;
+    c.split = blockIdx.x;
+    c.kvh = blockIdx.y;
+    c.b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_splits;
+
+    // ---- this split's token range: balanced whole tiles of the sequence
+    int L = __ldg(p.seqlens + c.b);
+    if (L < 0 || L > p.capacity) {
+        if (threadIdx.x == 0 && c.split == 0 && c.kvh == 0) raise_status(kStatusSeqlenBit);
+        L = L < 0 ? 0 : p.capacity;
+    }
+    const int n_tiles = (L + kTile - 1) / kTile;
+    const int base = n_tiles / S, rem = n_tiles % S;
+    const int t_begin = c.split * base + (c.split < rem ? c.split : rem);
+    const int t_count = base + (c.split < rem ? 1 : 0);
+    c.tok0 = t_begin * kTile;
+    c.tok1 = min((t_begin + t_count) * kTile, L);
+    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + kSub - 1) / kSub : 0;
+
+    c.bar0 = smem_u32(smem + kOffBars);
+    c.abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
+    c.cons_abort = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(c.full_bar(s), 1);
+            mbar_init(c.empty_bar(s), kConsumerWarps);
+        }
+        *c.abort_flag = 0;
+        *c.cons_abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        produce(c, &tmK, &tmV, lane);
+        return;
+    }
+
+    bool ok;
+    if constexpr (TC)
+        ok = consume_tc<T, G>(c, warp, lane);
+    else
+        ok = consume_simt<T, G>(c, warp, lane);
+    if (!ok) return;
     named_sync(1, kConsumerWarps * 32);
 
+    // ---- merge the four warp states of each head and write the split's state
+    const float* wacc = reinterpret_cast<const float*>(smem + kOffWAcc);
+    const float* wm = reinterpret_cast<const float*>(smem + kOffWM);
+    const float* wl = reinterpret_cast<const float*>(smem + kOffWL);
     const int d = threadIdx.x;   // 0 .. 127
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -420,8 +721,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             m_out = M * kLn2;
         }
-        const int64_t row = static_cast<int64_t>(b) * p.n_q_heads + kvh * G + g;
-        const int64_t idx = row * S + split;
+        const int64_t row = static_cast<int64_t>(c.b) * p.n_q_heads + c.kvh * G + g;
+        const int64_t idx = row * S + c.split;
         p.ws_u[idx * kHeadDim + d] = u;
         if (d == 0) {
             p.ws_m[idx] = m_out;
@@ -430,11 +731,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <typename T, int G>
+template <typename T, int G, bool TC>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
-    auto kern = fd_split_kernel<T, G>;
+    auto kern = fd_split_kernel<T, G, TC>;
     const size_t smem = split_smem_bytes();
     // one attribute call per (kernel, device): cheap and safe to repeat
     static thread_local int configured_device = -1;
@@ -452,8 +753,11 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, int group, int batch, int n_kv_heads, cudaStream_t stream) {
-#define FD_CASE(TT, GG) return launch_split_t<TT, GG>(tmK, tmV, p, batch, n_kv_heads, stream)
+                         int kv_dtype, int group, bool cuda_cores, int batch, int n_kv_heads,
+                         cudaStream_t stream) {
+#define FD_CASE(TT, GG)                                                                      \
+    return cuda_cores ? launch_split_t<TT, GG, false>(tmK, tmV, p, batch, n_kv_heads, stream) \
+                      : launch_split_t<TT, GG, true>(tmK, tmV, p, batch, n_kv_heads, stream)
     if (kv_dtype == 0) {
         switch (group) {
             case 1: FD_CASE(__half, 1);

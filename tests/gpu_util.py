@@ -45,7 +45,7 @@ class Guarded:
 
 
 def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=None,
-               n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True):
+               n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True, flags=0):
     """fd_decode through the C ABI; returns (out [B*Hq, D] f64, lse [B*Hq] f64, S)."""
     dev = q.device
     B, Hq, D = q.shape
@@ -59,6 +59,7 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
     desc = fd.make_desc(q, k, v, n_kv_heads=n_kv_heads, page_size=page_size, max_pages_per_seq=mp,
                         max_seqlen=int(seqlens_h.max()) if B else 0, n_splits=n_splits,
                         out_dtype=out_dtype)
+    desc.flags = flags
     S = n_splits if n_splits > 0 else fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
     assert S >= 1
     desc.n_splits = S

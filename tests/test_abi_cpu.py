@@ -144,7 +144,7 @@ def test_decode_rejects_bad_arguments_without_a_gpu(fd):
     assert call(_desc(fd, out_dtype=9)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, n_splits=129)) == fd.FD_ERR_UNSUPPORTED
     assert call(_desc(fd, k_stride_t=100)) == fd.FD_ERR_INVALID_ARG          # not 16-byte multiple
-    assert call(_desc(fd, flags=1)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, flags=2)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, kv_extent=0)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, page_size=12, max_pages_per_seq=4)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, page_size=4, max_pages_per_seq=4), bt=fake) == fd.FD_ERR_UNSUPPORTED

@@ -51,38 +51,48 @@ def test_tiny_mha_split_counts(n_splits):
 
 
 # ---------------------------------------------------------------- shapes
+PATHS = [0, fd.FD_FLAG_CUDA_CORES]   # tensor-core consumer (default), CUDA-core consumer
+
+
+@pytest.mark.parametrize("flags", PATHS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_group_sizes_and_dtypes(dtype, group):
+def test_group_sizes_and_dtypes(dtype, group, flags):
     B, Hkv, D, T = 2, 4, 128, 1500
     Hq = Hkv * group
     q = fd_inputs.randn((B, Hq, D), dtype, 100 + group, device=DEV)
     k, v = _cache(B, Hkv, T, D, dtype, 200 + group)
     sl = np.array([1500, 333], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
     for S in (0, 5):
-        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
-        ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
-        assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} {dtype} S={S}")
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S, flags=flags)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} {dtype} S={S} flags={flags}")
 
 
-def test_ragged_lengths_and_empty_splits():
+@pytest.mark.parametrize("flags", PATHS)
+def test_ragged_lengths_and_empty_splits(flags):
     """Lengths at every tile / stage edge, a length-1 and a length-0 sequence,
     and split counts that leave most splits empty ("Flash-Decoding ..." §8
-    functional checks)."""
+    functional checks).  The cache past each length is NaN: nothing of it may
+    reach the result."""
     lens = [0, 1, 2, 63, 64, 65, 127, 128, 129, 191, 255, 256, 257, 300, 1000, 1025]
     B, Hq, Hkv, D, T = len(lens), 8, 2, 128, 1100
     q = fd_inputs.randn((B, Hq, D), "f16", 301, device=DEV)
     k, v = _cache(B, Hkv, T, D, "f16", 302)
     sl = np.array(lens, dtype=np.int32)
+    for b, L in enumerate(lens):
+        k[b, :, L:] = float("nan")
+        v[b, :, L:] = float("nan")
     ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
     for S in (0, 1, 2, 3, 8, 9, 128):
-        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S, flags=flags)
         assert_parity(got_o, got_l, ref_o, ref_l, f"ragged S={S}")
         # the empty sequence: zero output and LSE = -inf exactly
         assert np.all(got_o[:Hq] == 0.0) and np.all(np.isneginf(got_l[:Hq]))
 
 
-def test_adversarial_large_scores():
+@pytest.mark.parametrize("flags", PATHS)
+def test_adversarial_large_scores(flags):
     """q scaled so that scores reach about +-80 and beyond: the max
     subtraction must hold in both kernels, no inf or NaN anywhere."""
     B, Hq, Hkv, D, T = 2, 16, 4, 128, 32768
@@ -94,7 +104,7 @@ def test_adversarial_large_scores():
         assert s.abs().max().item() > 75.0
         del s
         for S in (0, 1, 128):
-            got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+            got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S, flags=flags)
             ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
             assert_parity(got_o, got_l, ref_o, ref_l, f"gain={gain} S={S}")
             assert np.all(np.isfinite(got_l))
@@ -143,12 +153,21 @@ def _paged_problem(B, Hkv, D, ps, lens, dtype, seed, layout="HND", spare=7):
 
 @pytest.mark.parametrize("ps", [8, 16, 32, 64, 128, 256])
 def test_paged_page_sizes(ps):
+    """Paged pool with a shuffled block table; pages past each length are NaN."""
     B, Hkv, G, D = 3, 2, 8, 128
     Hq = Hkv * G
     lens = [3000, 17, 1025]
     pk, pv, bt = _paged_problem(B, Hkv, D, ps, lens, "bf16", 700 + ps)
     q = fd_inputs.randn((B, Hq, D), "bf16", 701, device=DEV)
     sl = np.array(lens, dtype=np.int32)
+    for b, L in enumerate(lens):          # poison every slot past the length
+        last = L // ps
+        if L % ps:
+            pk[int(bt[b, last]), :, L % ps:] = float("nan")
+            pv[int(bt[b, last]), :, L % ps:] = float("nan")
+        for jp in range(-(-L // ps), bt.shape[1]):
+            pk[int(bt[b, jp])] = float("nan")
+            pv[int(bt[b, jp])] = float("nan")
     ref_o, ref_l = oracle_all(q, pk, pv, sl, "bf16", Hkv, page_size=ps, block_table=bt)
     for S in (0, 3):
         got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=S)
