@@ -111,7 +111,8 @@ fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t
     const bool paged = d->page_size > 0;
     const int64_t n_tok = paged ? d->page_size : d->kv_extent;
     const int64_t n_outer = paged ? d->kv_extent : (d->batch > 0 ? d->batch : 1);
-    const int rows = paged ? (d->page_size < fdk::kSub ? d->page_size : fdk::kSub) : fdk::kSub;
+    const int rows = paged ? (d->page_size < fdk::kPagedBoxRows ? d->page_size : fdk::kPagedBoxRows)
+                           : fdk::kSub;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(n_tok),
                           static_cast<cuuint64_t>(d->n_kv_heads), static_cast<cuuint64_t>(n_outer)};
     // byte strides of dims 1..3; a stride of a size-1 dim is never used, but
@@ -164,6 +165,9 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.n_pages = paged ? static_cast<int32_t>(d->kv_extent) : 0;
     p.n_q_heads = d->n_q_heads;
     p.n_splits = S;
+    // whole 16-token units (8-token pages: 8), the paged box height, so a
+    // TMA box never crosses a page and paged and contiguous caches split alike
+    p.split_unit = paged && d->page_size < fdk::kSplitUnit ? d->page_size : fdk::kSplitUnit;
     p.score_scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
     char* ws = static_cast<char*>(workspace);
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);

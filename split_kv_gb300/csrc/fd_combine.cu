@@ -10,8 +10,9 @@
 // lse = -inf.  The loop order over splits is fixed, so results are bitwise
 // repeatable from run to run.
 //
-// One CTA of 128 threads per row, thread d owning output dim d; warp 0 first
-// reduces the per-split scalars.  The kernel is a few hundred bytes per row.
+// One CTA of 128 threads per row.  Launched with programmatic stream
+// serialization: it becomes resident while the split kernel runs and waits
+// (griddepcontrol.wait) for that kernel's states before reading them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -25,49 +26,71 @@ namespace {
 constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;
+constexpr int kWarps = kHeadDim / 32;   // 4
 
+// One CTA (4 warps) per row.  Thread (w, lane) accumulates dims 4*lane..+3
+// over splits i = w, w+4, ..., so the row's S x 128 partial outputs are all
+// in flight at once; the four warp partials are added in a fixed order.
 __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParams p) {
-    __shared__ float s_w[kMaxSplits];
+    __shared__ float s_m[kMaxSplits], s_w[kMaxSplits], s_l[kMaxSplits];
+    __shared__ float4 s_part[kWarps][32];
     __shared__ float s_M, s_L;
+    // let the next kernel in the stream get resident, then wait for the split
+    // kernel (programmatic dependent launch) before reading its states
+    grid_dependency_trigger();
+    grid_dependency_wait();
+
     const int row = blockIdx.x;
     const int t = threadIdx.x;
+    const int w = t >> 5, lane = t & 31;
     const int S = p.n_splits;
-    const float* mrow = p.ws_m + static_cast<int64_t>(row) * S;
-    const float* lrow = p.ws_l + static_cast<int64_t>(row) * S;
-
-    if (t < 32) {
+    if (t < S) {
+        s_m[t] = p.ws_m[static_cast<int64_t>(row) * S + t];
+        s_l[t] = p.ws_l[static_cast<int64_t>(row) * S + t];
+    }
+    __syncthreads();
+    if (w == 0) {
         float M = -INFINITY;
-        for (int i = t; i < S; i += 32) M = fmaxf(M, mrow[i]);
+        for (int i = lane; i < S; i += 32) M = fmaxf(M, s_m[i]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
         float L = 0.f;
-        for (int i = t; i < S; i += 32) {
-            const float m = mrow[i];
-            const float w = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2((m - M) * kLog2e);
-            s_w[i] = w;
-            L = fmaf(w, lrow[i], L);
+        for (int i = lane; i < S; i += 32) {
+            const float m = s_m[i];
+            const float wt = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2((m - M) * kLog2e);
+            s_w[i] = wt;
+            L = fmaf(wt, s_l[i], L);
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
-        if (t == 0) {
+        if (lane == 0) {
             s_M = M;
             s_L = L;
         }
     }
     __syncthreads();
-    const float M = s_M, L = s_L;
-    const float* urow = p.ws_u + static_cast<int64_t>(row) * S * kHeadDim + t;
-    float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;   // four chains, fixed order
-    int i = 0;
-    for (; i + 4 <= S; i += 4) {
-        u0 = fmaf(s_w[i + 0], urow[(i + 0) * kHeadDim], u0);
-        u1 = fmaf(s_w[i + 1], urow[(i + 1) * kHeadDim], u1);
-        u2 = fmaf(s_w[i + 2], urow[(i + 2) * kHeadDim], u2);
-        u3 = fmaf(s_w[i + 3], urow[(i + 3) * kHeadDim], u3);
+
+    const float4* urow = reinterpret_cast<const float4*>(p.ws_u + static_cast<int64_t>(row) * S * kHeadDim) + lane;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int i = w; i < S; i += kWarps) {
+        const float wt = s_w[i];
+        const float4 u = urow[i * (kHeadDim / 4)];
+        a.x = fmaf(wt, u.x, a.x);
+        a.y = fmaf(wt, u.y, a.y);
+        a.z = fmaf(wt, u.z, a.z);
+        a.w = fmaf(wt, u.w, a.w);
     }
-    for (; i < S; ++i) u0 = fmaf(s_w[i], urow[i * kHeadDim], u0);
-    const float u = (u0 + u1) + (u2 + u3);
+    s_part[w][lane] = a;
+    __syncthreads();
+
+    const float M = s_M, L = s_L;
     const bool empty = (M == -INFINITY) || !(L > 0.f);
+    // thread t writes dim t: component t % 4 of float4 t / 4
+    const int q4 = t >> 2, c = t & 3;
+    float u = 0.f;
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) u += reinterpret_cast<const float*>(&s_part[k][q4])[c];
     const float o = empty ? 0.f : u / L;
     const int64_t oi = static_cast<int64_t>(row) * kHeadDim + t;
     if (p.out_dtype == 2)
@@ -83,8 +106,7 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;
-    fd_combine_kernel<<<p.rows, kHeadDim, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(fd_combine_kernel, dim3(p.rows), dim3(kHeadDim), 0, stream, p);
 }
 
 }  // namespace fdk

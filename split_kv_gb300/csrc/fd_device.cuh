@@ -103,6 +103,18 @@ __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch (griddepcontrol).  trigger: kernels launched
+// after this one with programmatic stream serialization may start once every
+// CTA of this grid has triggered or exited.  wait: blocks until the grids this
+// one depends on have completed and their memory operations are visible.
+__device__ __forceinline__ void grid_dependency_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

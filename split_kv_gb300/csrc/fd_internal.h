@@ -9,12 +9,13 @@
 namespace fdk {
 
 constexpr int kHeadDim = 128;     // D
-constexpr int kTile = 128;        // split granularity in tokens (the planner's KV block)
 constexpr int kSub = 64;          // tokens per pipeline stage
 constexpr int kStages = 3;        // pipeline depth (stages in flight per CTA)
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + one TMA producer warp
 constexpr int kHalfBytes = kSub * 128;                // one [kSub tokens x 64 dims] 16-bit box
+constexpr int kSplitUnit = 16;                        // split ranges are whole 16-token units
+constexpr int kPagedBoxRows = 16;                     // paged boxes: at most one unit of one page
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
 
 // Device status bits (sticky until fd_device_status(clear)).
@@ -34,6 +35,7 @@ struct SplitParams {
     int32_t n_pages;                // paged pool size
     int32_t n_q_heads;
     int32_t n_splits;
+    int32_t split_unit;             // split ranges are whole units of this many tokens
     float score_scale_log2;         // log2(e) / sqrt(D)
     float* ws_u;                    // [rows][n_splits][D]
     float* ws_m;                    // [rows][n_splits]
@@ -52,6 +54,27 @@ struct CombineParams {
 };
 
 size_t split_smem_bytes();
+
+// Launches `kern` with programmatic stream serialization, so that it may
+// start while the previous kernel in the stream finishes; the kernel itself
+// waits (griddepcontrol.wait) before touching anything that kernel wrote.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       const Args&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 // Launchers return cudaGetLastError() after the launch.
 // cuda_cores selects the CUDA-core (FP32 FMA) consumer instead of the tensor-core one.

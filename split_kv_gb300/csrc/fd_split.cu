@@ -15,8 +15,8 @@
 //  - Warp 4 is a TMA producer: per 64-token stage it issues four 2-D boxes
 //    [64 tokens x 64 dims] (K low/high half, V low/high half) with 128-byte
 //    swizzle into a 3-stage ring, completing on the stage's "full" mbarrier.
-//    Contiguous caches use one box per half; paged caches one box per page
-//    (page_size >= 8), resolved through the block table a stage ahead.
+//    Contiguous caches use one box per half; paged caches 16-row boxes (8 for
+//    8-token pages) resolved through the block table a stage ahead.
 //  - Warps 0-3 consume.  Each warp owns 16 of a stage's 64 rows and keeps its
 //    own running (m, l, acc) per query head; the four warp states are merged
 //    exactly at the end of the split (the same max-subtracted rule).
@@ -167,14 +167,10 @@ struct SplitCtx {
 __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tmK,
                                         const CUtensorMap* tmV, int lane) {
     const SplitParams& p = *c.p;
-    if (lane == 0) {
-        prefetch_tensormap(tmK);
-        prefetch_tensormap(tmV);
-    }
     const uint64_t policy = policy_evict_first();
     const bool paged = p.page_size != 0;
-    const int rows = paged ? min(kSub, p.page_size) : kSub;   // tokens per box
-    const int nbox = kSub / rows;                              // boxes per half per stage
+    const int rows = paged ? min(kPagedBoxRows, p.page_size) : kSub;   // tokens per box
+    const int nbox = kSub / rows;                                        // boxes per half per stage
     // physical page of box `lane` of sub-tile i (paged); -1 reads zeros
     auto page_of = [&](int i) -> int {
         const int t = c.tok0 + i * kSub + lane * rows;
@@ -657,24 +653,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
 
-    // ---- this split's token range: balanced whole tiles of the sequence
-    int L = __ldg(p.seqlens + c.b);
-    if (L < 0 || L > p.capacity) {
-        if (threadIdx.x == 0 && c.split == 0 && c.kvh == 0) raise_status(kStatusSeqlenBit);
-        L = L < 0 ? 0 : p.capacity;
-    }
-    const int n_tiles = (L + kTile - 1) / kTile;
-    const int base = n_tiles / S, rem = n_tiles % S;
-    const int t_begin = c.split * base + (c.split < rem ? c.split : rem);
-    const int t_count = base + (c.split < rem ? 1 : 0);
-    c.tok0 = t_begin * kTile;
-    c.tok1 = min((t_begin + t_count) * kTile, L);
-    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + kSub - 1) / kSub : 0;
-
     c.bar0 = smem_u32(smem + kOffBars);
     c.abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
     c.cons_abort = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);
-
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
@@ -685,6 +666,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         *c.cons_abort = 0;
         fence_barrier_init();
     }
+    if (warp == kConsumerWarps && lane == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    // Programmatic dependent launch: let the combine kernel that follows get
+    // resident now, and wait for whatever preceded this kernel in the stream
+    // to finish (and its writes to land) before reading any input.
+    grid_dependency_trigger();
+    grid_dependency_wait();
+
+    // ---- this split's token range: the sequence cut into S balanced ranges
+    // of whole 16-token units (8 for 8-token pages), so no TMA box straddles
+    // a page and a paged cache splits exactly like a contiguous one
+    int L = __ldg(p.seqlens + c.b);
+    if (L < 0 || L > p.capacity) {
+        if (threadIdx.x == 0 && c.split == 0 && c.kvh == 0) raise_status(kStatusSeqlenBit);
+        L = L < 0 ? 0 : p.capacity;
+    }
+    const int unit = p.split_unit;
+    const int n_units = (L + unit - 1) / unit;
+    const int base = n_units / S, rem = n_units % S;
+    const int u_begin = c.split * base + (c.split < rem ? c.split : rem);
+    const int u_count = base + (c.split < rem ? 1 : 0);
+    c.tok0 = u_begin * unit;
+    c.tok1 = min((u_begin + u_count) * unit, L);
+    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + kSub - 1) / kSub : 0;
     __syncthreads();
 
     if (warp == kConsumerWarps) {
@@ -747,9 +754,8 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    dim3 grid(p.n_splits, n_kv_heads, batch);
-    kern<<<grid, kThreads, smem, stream>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads, batch), dim3(kThreads), smem, stream,
+                      tmK, tmV, p);
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
