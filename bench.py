@@ -137,14 +137,19 @@ def _barrier(ws):
         dist.barrier()
 
 
-def _max_over_ranks(x: float, ws: int) -> float:
+def aggregate_ranks(ms_local: float, bytes_local: float, ws: int):
+    """Whole-job numbers of N replicas: the step time is the slowest rank's,
+    the bytes are every rank's.  Works on NCCL (CUDA tensors) and gloo."""
     if ws == 1:
-        return x
+        return ms_local, bytes_local
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    b = torch.tensor([bytes_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
 
 
 def _traffic_from_profile(src_hash: str):
@@ -314,11 +319,11 @@ def run_gpu(args):
     _barrier(ws)
     clocks = sampler.stop() if sampler else None
     ms_local = e0.elapsed_time(e1) / args.steps
-    ms = _max_over_ranks(ms_local, ws)
     fd.check(fd.fd_device_status(stream), "device status after timing")
 
     kv_bytes_layer = B * Hkv * T * D * 2 * 2
-    value = ws * n_layers * kv_bytes_layer / (ms * 1e-3) / 1e9
+    ms, job_bytes = aggregate_ranks(ms_local, float(n_layers * kv_bytes_layer), ws)
+    value = job_bytes / (ms * 1e-3) / 1e9
     us_layer = ms * 1e3 / n_layers
 
     # ---- roofline of fd_split: per-launch CUDA events around the kernel alone
@@ -391,6 +396,44 @@ def run_gpu(args):
         e2e = {"value": ws * kv_bytes_layer / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "step": "one layer: H2D q/K/V/seqlens, fd_decode, D2H out/lse"}
+
+        # serving form: the cache stays resident; per step only q, the new
+        # token's K/V row of every KV head and the lengths come from the host
+        hk_new = ks[0][:, :, T - 1:T].cpu().pin_memory()
+        hv_new = vs[0][:, :, T - 1:T].cpu().pin_memory()
+        dk.copy_(ks[0])
+        dv.copy_(vs[0])
+
+        def serve_step():
+            dq.copy_(hq, non_blocking=True)
+            dk[:, :, T - 1:T].copy_(hk_new, non_blocking=True)
+            dv[:, :, T - 1:T].copy_(hv_new, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            rc = fd.fd_decode(desc, dq, dk, dv, dsl, None, dout, dl, workspace, wsb, stream=sp)
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode")
+            ho.copy_(dout, non_blocking=True)
+            hl.copy_(dl, non_blocking=True)
+
+        for _ in range(3):
+            serve_step()
+        torch.cuda.synchronize()
+        n_srv = max(10, min(200, args.steps))
+        t0 = time.perf_counter()
+        a0.record(stream)
+        for _ in range(n_srv):
+            serve_step()
+            stream.synchronize()          # the caller reads the result every step
+        a1.record(stream)
+        torch.cuda.synchronize()
+        srv_ms = a0.elapsed_time(a1) / n_srv
+        srv_wall_ms = (time.perf_counter() - t0) * 1e3 / n_srv
+        e2e["resident_cache"] = {
+            "value": ws * kv_bytes_layer / (srv_wall_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": srv_wall_ms, "device_ms_per_step": srv_ms,
+            "h2d_bytes_per_step": hq.numel() * 2 + hk_new.numel() * 2 + hv_new.numel() * 2 + hsl.numel() * 4,
+            "d2h_bytes_per_step": d2h,
+            "step": "one layer, cache resident: H2D q + new K/V row + seqlens, fd_decode, D2H out/lse, host sync"}
 
     # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
     cpu = None

@@ -71,6 +71,11 @@ typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
  * same memory pipeline, same results within the stated tolerance; kept for
  * comparison and profiling. */
 #define FD_FLAG_CUDA_CORES 1
+/* Test hook for failure detection, never for production: the split kernel
+ * does not request its first K/V stage, so the wait for it runs out after its
+ * limit (about 2 s), the kernel records FD_ERR_DEVICE_TIMEOUT in the device
+ * status word and returns without a fault; out and lse are then unspecified. */
+#define FD_FLAG_TEST_DROP_FIRST_STAGE (1 << 16)
 
 /* Problem descriptor: plain data, filled by the caller, read (never kept) by
  * each call.  Strides are in ELEMENTS; the head dimension is always contiguous.
@@ -104,7 +109,7 @@ typedef struct fd_desc {
     int32_t max_pages_per_seq;  /* paged: row length (stride) of block_table */
     int32_t max_seqlen;         /* host-known upper bound of seqlens[]; used when n_splits <= 0 */
     int32_t n_splits;           /* >= 1: use it; <= 0: plan it with fd_plan's rule from max_seqlen */
-    int32_t flags;              /* 0, or FD_FLAG_CUDA_CORES */
+    int32_t flags;              /* 0, or FD_FLAG_* bits */
     int32_t reserved;           /* must be 0 */
 } fd_desc;
 

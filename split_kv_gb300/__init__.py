@@ -38,6 +38,7 @@ FD_MAX_SPLITS = 128
 FD_TILE_TOKENS = 128
 FD_STATIC_WORKSPACE_BYTES = 8 << 20
 FD_FLAG_CUDA_CORES = 1
+FD_FLAG_TEST_DROP_FIRST_STAGE = 1 << 16
 
 LIB_PATH = _build.LIB_PATH
 

@@ -41,7 +41,8 @@ bool stride_ok(int64_t s) { return s >= 0 && s % 8 == 0 && s < (int64_t(1) << 38
 // done by the callers, which know which pointers they use.
 fd_status check_desc(const fd_desc* d) {
     if (d == nullptr) return FD_ERR_INVALID_ARG;
-    if ((d->flags & ~FD_FLAG_CUDA_CORES) != 0 || d->reserved != 0) return FD_ERR_INVALID_ARG;
+    if ((d->flags & ~(FD_FLAG_CUDA_CORES | FD_FLAG_TEST_DROP_FIRST_STAGE)) != 0 || d->reserved != 0)
+        return FD_ERR_INVALID_ARG;
     if (d->batch < 0 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1)
         return FD_ERR_INVALID_ARG;
     if (d->n_q_heads % d->n_kv_heads != 0) return FD_ERR_INVALID_ARG;
@@ -168,6 +169,7 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     // whole 16-token units (8-token pages: 8), the paged box height, so a
     // TMA box never crosses a page and paged and contiguous caches split alike
     p.split_unit = paged && d->page_size < fdk::kSplitUnit ? d->page_size : fdk::kSplitUnit;
+    p.drop_first_stage = (d->flags & FD_FLAG_TEST_DROP_FIRST_STAGE) != 0 ? 1 : 0;
     p.score_scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
     char* ws = static_cast<char*>(workspace);
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);

@@ -36,6 +36,7 @@ struct SplitParams {
     int32_t n_q_heads;
     int32_t n_splits;
     int32_t split_unit;             // split ranges are whole units of this many tokens
+    int32_t drop_first_stage;       // test hook: never request stage 0 (the wait for it times out)
     float score_scale_log2;         // log2(e) / sqrt(D)
     float* ws_u;                    // [rows][n_splits][D]
     float* ws_m;                    // [rows][n_splits]

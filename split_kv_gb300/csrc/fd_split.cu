@@ -185,6 +185,7 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
     };
     int page_next = paged ? page_of(0) : 0;
     int issued = 0;
+    const int first = p.drop_first_stage ? 1 : 0;   // test hook: stage 0 is never requested
 #pragma unroll 1
     for (int i = 0; i < c.n_sub; ++i) {
         const int st = i % kStages;
@@ -197,6 +198,10 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
         const int tok = c.tok0 + i * kSub;
         const uint32_t dst = smem_u32(c.smem + st * kStageBytes);
         const uint32_t bar = c.full_bar(st);
+        if (i < first) {
+            if (paged) page_next = page_of(i + 1);
+            continue;
+        }
         if (lane == 0) mbar_arrive_expect_tx(bar, kStageBytes);
         __syncwarp();
         if (!paged) {
@@ -220,7 +225,7 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
     // Drain: the last sub-tile issued into each stage must have landed before
     // this CTA may exit (a no-op unless a consumer gave up).
     if (lane == 0) {
-        for (int i = max(0, issued - kStages); i < issued; ++i)
+        for (int i = max(first, issued - kStages); i < issued; ++i)
             wait_or_flag(c.full_bar(i % kStages), (i / kStages) & 1);
     }
 }

@@ -363,3 +363,59 @@ def test_sweep_plans_and_sampled_rows(batch):
         assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"sweep B={batch} ctx={ctx} S={S}")
         del k, v
         torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- LSE chaining, bounded waits
+def test_lse_chaining_two_halves_merged_externally():
+    """Decode the two halves of each sequence separately, then merge the two
+    returned (out, lse) states with fd_combine_states: the result must equal
+    the one-pass decode and the oracle ("Flash-Decoding ..." §8: return LSE
+    and merge two halves externally, which catches base and scale bugs)."""
+    B, Hq, Hkv, D, T, half = 2, 16, 4, 128, 6000, 2048
+    q = fd_inputs.randn((B, Hq, D), "bf16", 1101, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "bf16", 1102)
+    sl = np.array([6000, 5000], dtype=np.int32)
+    o_full, l_full, _ = run_decode(q, k, v, sl)
+    o1, l1, _ = run_decode(q, k[:, :, :half], v[:, :, :half], np.array([half, half], dtype=np.int32))
+    o2, l2, _ = run_decode(q, k[:, :, half:], v[:, :, half:], sl - half)
+    rows = B * Hq
+    m = np.stack([l1, l2], axis=1)                 # natural-log LSE as the state max
+    ell = np.ones((rows, 2))
+    u = np.stack([o1, o2], axis=1)
+    desc = fd.make_desc(q, k, v, n_splits=2)
+    ws, wsb = _states_workspace(desc, 2, m, ell, u)
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    fd.check(fd.fd_combine_states(desc, ws, out, lse, wsb))
+    torch.cuda.synchronize()
+    got_o = out.cpu().double().numpy().reshape(rows, D)
+    got_l = lse.cpu().double().numpy().reshape(-1)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "bf16", Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, "two halves merged")
+    np.testing.assert_allclose(got_o, o_full, rtol=0, atol=2e-5)
+    np.testing.assert_allclose(got_l, l_full, rtol=0, atol=2e-5)
+
+
+def test_bounded_wait_reports_timeout_and_the_context_survives():
+    """The test hook drops the first K/V stage: the kernel's bounded wait runs
+    out, the status word reports FD_ERR_DEVICE_TIMEOUT, nothing faults, and
+    the next call on the same context is correct."""
+    import time
+    B, Hq, Hkv, D, T = 1, 8, 8, 128, 300
+    q = fd_inputs.randn((B, Hq, D), "f16", 1201, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "f16", 1202)
+    sl_h = np.array([T], dtype=np.int32)
+    seqlens = torch.from_numpy(sl_h).to(DEV)
+    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=1)
+    desc.flags = fd.FD_FLAG_TEST_DROP_FIRST_STAGE
+    ws = torch.empty(fd.fd_workspace_size(desc, 1), dtype=torch.uint8, device=DEV)
+    out = torch.zeros(B, Hq, D, dtype=torch.float32, device=DEV)
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    t0 = time.time()
+    fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, None, ws))
+    assert fd.fd_device_status(clear=True) == fd.FD_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 60
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1)
+    ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv)
+    assert_parity(got_o, got_l, ref_o, ref_l, "after a timed-out call")
