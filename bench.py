@@ -51,6 +51,8 @@ def _args():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every call from Python instead of replaying a captured CUDA graph")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
     ap.add_argument("--workload", default=None,
@@ -293,10 +295,10 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
-    def step():
+    def step(handle=sp):
         for i in range(n_layers):
             rc = fd.fd_decode(desc, qs[i], ks[i], vs[i], seqlens, None, out[i], lse[i], workspace,
-                              wsb, stream=sp)
+                              wsb, stream=handle)
             if rc != 0:
                 raise fd.FdError(rc, "fd_decode")
 
@@ -304,6 +306,13 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize()
     fd.check(fd.fd_device_status(stream), "device status after warm-up")
+    # one step (the 32 fd_decode calls) captured once and replayed: the same
+    # kernels with the same arguments, without Python launch overhead
+    graph, graph_note = _capture(lambda h: step(h), dev, stream, args.eager)
+    run_step = graph.replay if graph is not None else step
+    for _ in range(2):
+        run_step()
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -313,7 +322,7 @@ def run_gpu(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     _barrier(ws)
@@ -455,6 +464,7 @@ def run_gpu(args):
             "clocks": clocks, "gpu_launches": 2 * n_layers * args.steps,
             "workspace_bytes": wsb, "num_sms": fd.fd_num_sms(),
             "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores",
+            "launch": graph_note,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -462,19 +472,57 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def _capture(body, dev, stream, eager: bool):
+    """Capture body(stream_handle) into a CUDA graph (fd_decode allocates and
+    synchronises nothing, so it is capturable).  Returns (graph or None, note)."""
+    import torch
+    if eager:
+        return None, "eager"
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            body(cap.cuda_stream)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        return g, "cuda_graph"
+    except Exception as e:  # report, and time the eager launches instead
+        torch.cuda.synchronize()
+        return None, f"eager (graph capture failed: {type(e).__name__})"
+
+
 # ---------------------------------------------------------------- other workloads
-def _time_calls(fn, n_sets, iters, warmup, stream):
+def _time_calls(fn, n_sets, iters, warmup, stream, dev, eager):
+    """Device time per call; the calls over all input sets are replayed as
+    one captured graph unless eager."""
     import torch
     for i in range(warmup):
-        fn(i % n_sets)
+        fn(i % n_sets, stream.cuda_stream)
     torch.cuda.synchronize()
+
+    def body(h):
+        for j in range(n_sets):
+            fn(j, h)
+
+    graph, note = _capture(body, dev, stream, eager)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph is not None:
+        reps = max(2, -(-iters // n_sets))
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * n_sets), note
     e0.record(stream)
     for i in range(iters):
-        fn(i % n_sets)
+        fn(i % n_sets, stream.cuda_stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / iters
+    return e0.elapsed_time(e1) / iters, note
 
 
 def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
@@ -566,15 +614,14 @@ def run_suite(args):
             out = torch.empty(B, c["n_q_heads"], c["head_dim"], dtype=torch.float32, device=dev)
             lse = torch.empty(B, c["n_q_heads"], dtype=torch.float32, device=dev)
 
-            def call(j):
+            def call(j, h):
                 _, q, k, v, bt = sets[j]
-                rc = fd.fd_decode(descs[j], q, k, v, seqlens, bt, out, lse, ws, wsb,
-                                  stream=stream.cuda_stream)
+                rc = fd.fd_decode(descs[j], q, k, v, seqlens, bt, out, lse, ws, wsb, stream=h)
                 if rc != 0:
                     raise fd.FdError(rc, "fd_decode")
 
             iters = max(20, min(400, int(2e9 / max(kv_bytes, 1))))
-            ms = _time_calls(call, n_sets, iters, max(3, args.warmup), stream)
+            ms, note = _time_calls(call, n_sets, iters, max(3, args.warmup), stream, dev, args.eager)
             results[label] = (S, ms)
         fd.check(fd.fd_device_status(stream), "device status")
         S, ms = results["planned"]
@@ -582,7 +629,7 @@ def run_suite(args):
                 "n_kv_heads": c["n_kv_heads"], "kv_dtype": c["dtype"], "n_splits": S,
                 "us_per_call": ms * 1e3, "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
                 "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
-                "input_sets": n_sets, "kv_bytes": kv_bytes,
+                "input_sets": n_sets, "kv_bytes": kv_bytes, "launch": note,
                 "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores"}
         if "unsplit" in results:
             S1, ms1 = results["unsplit"]

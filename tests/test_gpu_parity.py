@@ -419,3 +419,34 @@ def test_bounded_wait_reports_timeout_and_the_context_survives():
     got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1)
     ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv)
     assert_parity(got_o, got_l, ref_o, ref_l, "after a timed-out call")
+
+
+def test_fd_decode_replays_from_a_cuda_graph():
+    """fd_decode allocates and synchronises nothing, so it can be captured in
+    a CUDA graph; replays after the inputs change in place are correct."""
+    B, Hq, Hkv, D, T = 2, 32, 8, 128, 3000
+    q = fd_inputs.randn((B, Hq, D), "f16", 1301, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "f16", 1302)
+    sl_h = np.array([3000, 1234], dtype=np.int32)
+    seqlens = torch.from_numpy(sl_h).to(DEV)
+    desc = fd.make_desc(q, k, v, max_seqlen=T)
+    desc.n_splits = fd.fd_plan(B, Hq, Hkv, D, sl_h)
+    wsb = fd.fd_workspace_size(desc, desc.n_splits)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=DEV)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+    fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, lse, ws))   # eager warm-up
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, lse, ws, stream=cap))
+    for seed in (1303, 1304):
+        q.copy_(fd_inputs.randn((B, Hq, D), "f16", seed, device=DEV))
+        k.copy_(fd_inputs.randn((B, Hkv, T, D), "f16", seed + 10, device=DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv)
+        assert_parity(out.cpu().double().numpy().reshape(B * Hq, D),
+                      lse.cpu().double().numpy().reshape(-1), ref_o, ref_l, f"graph replay {seed}")
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
