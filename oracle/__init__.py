@@ -72,8 +72,8 @@ def _load():
         lib.fdo_plan.restype = ctypes.c_int
         lib.fdo_plan.argtypes = [i64, i64, i64, ctypes.c_int, vp]
         lib.fdo_decode.restype = ctypes.c_int
-        lib.fdo_decode.argtypes = [i32, i32, i32, i32, i32,
-                                   vp, i64, i64,
+        lib.fdo_decode.argtypes = [i32, i32, i32, i32, i32, i32,
+                                   vp, i64, i64, i64,
                                    vp, i64, i64, i64,
                                    vp, i64, i64, i64,
                                    vp,
@@ -187,20 +187,24 @@ def _bits(a) -> np.ndarray:
 
 def decode(q, k, v, seqlens, *, dtype: str, n_kv_heads: int,
            page_size: int = 0, block_table=None, rows=None, n_threads: int = 0):
-    """Decode attention in fp64 for every (sequence, query head) row.
+    """Decode attention in fp64 for every (sequence, query position, query head) row.
 
-    q: [B, Hq, D] 16-bit; contiguous k, v: [B, Hkv, T, D] (any 4-D strided
+    q: [B, Hq, D] (one query per sequence) or [B, q_len, Hq, D] (a short query
+    block: position i sees the first L_b - q_len + 1 + i keys) 16-bit;
+    contiguous k, v: [B, Hkv, T, D] (any 4-D strided
     view whose last dim is contiguous); paged k, v: pool [P, Hkv, page, D] (or
     any 4-D view [P, Hkv, page, D] with contiguous last dim) with block_table
     [B, max_pages] int32.  dtype: 'f16' or 'bf16'.  rows: optional flat row
-    indices b*Hq + h.  Returns (out[n, D] float64, lse[n] float64).
+    indices (b*q_len + i)*Hq + h.  Returns (out[n, D] float64, lse[n] float64).
     """
     dt = {"f16": 0, "bf16": 1}[dtype]
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
-    B, Hq, D = qb.shape
+    if qb.ndim == 3:
+        qb = qb[:, None]
+    B, q_len, Hq, D = qb.shape
     if qb.strides[-1] != 2 or kb.strides[-1] != 2 or vb.strides[-1] != 2:
         raise ValueError("last dim must be contiguous")
-    qs = [s // 2 for s in qb.strides]
+    qs = [s // 2 for s in qb.strides]        # b, i, h, d
     ks = [s // 2 for s in kb.strides]
     vs = [s // 2 for s in vb.strides]
     sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
@@ -215,12 +219,12 @@ def decode(q, k, v, seqlens, *, dtype: str, n_kv_heads: int,
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n = rows.shape[0]
     else:
-        n = B * Hq
+        n = B * q_len * Hq
     out = np.empty((n, D))
     lse = np.empty(n)
     rc = _load().fdo_decode(
-        B, Hq, int(n_kv_heads), D, dt,
-        qb.ctypes.data, qs[0], qs[1],
+        B, Hq, int(n_kv_heads), D, dt, q_len,
+        qb.ctypes.data, qs[0], qs[1], qs[2],
         kb.ctypes.data, ks[0], ks[1], ks[2],
         vb.ctypes.data, vs[0], vs[1], vs[2],
         _ptr(sl),

@@ -236,7 +236,13 @@ int fdo_plan(int64_t work_items, int64_t slots, int64_t n_kv_blocks, int max_spl
     return 1;
 }
 
-// Decode attention for a batch, one query row per (sequence b, query head h):
+// Decode attention for a batch: q_len query rows per sequence (1 for plain
+// decode; 2-8 for the short query blocks of speculative verification,
+// "Flash-Decoding ..." §7 and §9), each with its own visibility ([DKV] §06):
+//  * query position i (0 <= i < q_len) of sequence b sees keys
+//    0 .. L_b - q_len + i, i.e. the first L_b - q_len + 1 + i keys (the
+//    block's own tokens are already in the cache, causally ordered); none if
+//    that count is <= 0;
 //  * query head h reads KV head h / (n_q_heads / n_kv_heads)  (grouped-query
 //    attention with consecutive query heads sharing a KV head; [FD] §1 GQA note);
 //  * sequence b sees keys 0 .. seqlens[b]-1;
@@ -247,25 +253,25 @@ int fdo_plan(int64_t work_items, int64_t slots, int64_t n_kv_blocks, int max_spl
 //    ([FD] §7 paged row; [DKV] §02: splits are logical ranges resolved through
 //    the block table), and the same for v;
 //  * s_j = q.k_j / sqrt(head_dim); out = softmax(s) V, lse = natural-log LSE.
-// q is read at q + b*q_sb + h*q_sh.  dtype 0 = fp16, 1 = bf16 (raw bits).
-// rows (nullable) lists flat row indices b*n_q_heads + h to evaluate; out/lse
-// then hold n_rows results in that order.  Rows run on n_threads host threads
-// (<= 0: all hardware threads).
+// q is read at q + b*q_sb + i*q_st + h*q_sh.  dtype 0 = fp16, 1 = bf16 (raw
+// bits).  Rows are numbered r = (b*q_len + i)*n_q_heads + h; rows (nullable)
+// lists the rows to evaluate, and out/lse then hold n_rows results in that
+// order.  Rows run on n_threads host threads (<= 0: all hardware threads).
 int fdo_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-               int32_t dtype,
-               const uint16_t* q, int64_t q_sb, int64_t q_sh,
+               int32_t dtype, int32_t q_len,
+               const uint16_t* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
                const uint16_t* k, int64_t k_sb, int64_t k_sh, int64_t k_st,
                const uint16_t* v, int64_t v_sb, int64_t v_sh, int64_t v_st,
                const int32_t* seqlens,
                int32_t page_size, const int32_t* block_table, int32_t max_pages_per_seq,
                const int64_t* rows, int64_t n_rows,
                double* out, double* lse, int32_t n_threads) {
-    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return -1;
+    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || q_len <= 0) return -1;
     if (n_q_heads % n_kv_heads != 0) return -1;
     if (dtype != 0 && dtype != 1) return -1;
     if (!q || !k || !v || !seqlens || !out || !lse) return -1;
     if (page_size < 0 || (page_size > 0 && (!block_table || max_pages_per_seq <= 0))) return -1;
-    const int64_t total = static_cast<int64_t>(batch) * n_q_heads;
+    const int64_t total = static_cast<int64_t>(batch) * q_len * n_q_heads;
     const int64_t count = rows ? n_rows : total;
     if (count < 0) return -1;
     for (int64_t r = 0; rows && r < count; ++r)
@@ -278,11 +284,13 @@ int fdo_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t hea
         std::vector<double> qd(D), s, acc;
         for (int64_t r = first; r < last; ++r) {
             const int64_t row = rows ? rows[r] : r;
-            const int64_t b = row / n_q_heads;
             const int64_t h = row % n_q_heads;
+            const int64_t i = (row / n_q_heads) % q_len;
+            const int64_t b = row / (static_cast<int64_t>(n_q_heads) * q_len);
             const int64_t g = h / group;
-            const int64_t L = std::max<int32_t>(seqlens[b], 0);
-            for (int d = 0; d < D; ++d) qd[d] = to_double(q[b * q_sb + h * q_sh + d], dtype);
+            const int64_t L = std::max<int64_t>(static_cast<int64_t>(seqlens[b]) - q_len + 1 + i, 0);
+            for (int d = 0; d < D; ++d)
+                qd[d] = to_double(q[b * q_sb + i * q_st + h * q_sh + d], dtype);
             // element offset of key / value j of (b, g), before the head-dim index
             auto k_off = [&](int64_t j) -> int64_t {
                 if (page_size == 0) return b * k_sb + g * k_sh + j * k_st;

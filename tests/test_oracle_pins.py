@@ -340,3 +340,45 @@ def test_plan_c_and_python_statements_agree():
         nb = int(rng.integers(0, 2200))
         ms = int(rng.integers(1, 160))
         assert oracle.plan(work, slots, nb, ms) == oracle.num_splits_ref(work, slots, nb, ms)
+
+
+# --------------------------------------------------------------------------
+# short query blocks: position i of q_len sees the first L - q_len + 1 + i keys
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("q_len", [2, 4, 8])
+def test_query_block_reduces_to_single_queries_on_prefixes(q_len):
+    rng = np.random.default_rng(40 + q_len)
+    B, Hq, Hkv, T, D = 3, 8, 2, 70, 16
+    q = rng.standard_normal((B, q_len, Hq, D)).astype(np.float16)
+    k = rng.standard_normal((B, Hkv, T, D)).astype(np.float16)
+    v = rng.standard_normal((B, Hkv, T, D)).astype(np.float16)
+    sl = np.array([70, 9, 3], dtype=np.int32)
+    out, lse = oracle.decode(q, k, v, sl, dtype="f16", n_kv_heads=Hkv)
+    out = out.reshape(B, q_len, Hq, D)
+    lse = lse.reshape(B, q_len, Hq)
+    for i in range(q_len):
+        prefix = np.maximum(sl - q_len + 1 + i, 0).astype(np.int32)
+        o1, l1 = oracle.decode(np.ascontiguousarray(q[:, i]), k, v, prefix, dtype="f16", n_kv_heads=Hkv)
+        assert np.array_equal(out[:, i].reshape(-1, D), o1)
+        assert np.array_equal(lse[:, i].reshape(-1), l1)
+    # sequence 2 holds 3 tokens: with q_len > 3 its first positions see nothing
+    for i in range(q_len):
+        if 3 - q_len + 1 + i <= 0:
+            assert np.all(out[2, i] == 0.0) and np.all(np.isneginf(lse[2, i]))
+
+
+def test_query_block_against_scipy():
+    rng = np.random.default_rng(77)
+    q_len, Hq, D, L = 4, 2, 8, 11
+    q = rng.standard_normal((1, q_len, Hq, D)).astype(np.float16)
+    k = rng.standard_normal((1, 1, L, D)).astype(np.float16)
+    v = rng.standard_normal((1, 1, L, D)).astype(np.float16)
+    out, lse = oracle.decode(q, k, v, [L], dtype="f16", n_kv_heads=1)
+    kd, vd, qd = k[0, 0].astype(np.float64), v[0, 0].astype(np.float64), q[0].astype(np.float64)
+    for i in range(q_len):
+        n = L - q_len + 1 + i
+        for h in range(Hq):
+            s = kd[:n] @ qd[i, h] / math.sqrt(D)
+            r = i * Hq + h
+            np.testing.assert_allclose(out[r], scipy.special.softmax(s) @ vd[:n], rtol=1e-12, atol=1e-13)
+            assert lse[r] == pytest.approx(scipy.special.logsumexp(s), abs=1e-12)
