@@ -36,8 +36,19 @@
  *    share a KV head).  The G query rows of a group are packed into one CTA so
  *    each K/V tile is read from HBM once per group ("Flash-Decoding ...", §1
  *    GQA note).
- *  - Supported shapes: head_dim 128; G in {1, 2, 4, 8}; kv_dtype FD_F16 or
- *    FD_BF16; 1 <= n_splits <= 128.  Other shapes return FD_ERR_UNSUPPORTED.
+ *  - Query blocks: q_len query positions per sequence (1 for a plain decode
+ *    step; 2-16 for the short query blocks of speculative verification,
+ *    "Flash-Decoding ...", §7 and §9).  Position i of sequence b sees the
+ *    first seqlens[b] - q_len + 1 + i keys (the block's own tokens are
+ *    already in the cache, in order); a position that sees no key gets
+ *    out = 0 and lse = -inf.  Every (position, head) of a KV head's group is
+ *    one column of the CTA's tensor-core tile: up to 16 columns per CTA; a
+ *    group with more columns uses ceil(G*q_len/16) CTAs per split, each
+ *    reading the split's K/V once.
+ *  - Supported shapes: head_dim 128; G = n_q_heads / n_kv_heads and q_len
+ *    with G*q_len <= 256 and q_len <= 16 (with FD_FLAG_CUDA_CORES: G in
+ *    {1, 2, 4, 8} and q_len = 1); kv_dtype FD_F16 or FD_BF16;
+ *    1 <= n_splits <= 128.  Other shapes return FD_ERR_UNSUPPORTED.
  */
 #ifndef FD_H_
 #define FD_H_
@@ -49,7 +60,7 @@
 extern "C" {
 #endif
 
-#define FD_ABI_VERSION 1
+#define FD_ABI_VERSION 2
 #define FD_MAX_SPLITS 128   /* the split-count heuristic's cap ("Flash-Decoding ...", §6) */
 #define FD_TILE_TOKENS 128  /* split ranges are whole 128-token tiles; the planner's KV block */
 
@@ -80,7 +91,9 @@ typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
 /* Problem descriptor: plain data, filled by the caller, read (never kept) by
  * each call.  Strides are in ELEMENTS; the head dimension is always contiguous.
  *
- * q        [batch, n_q_heads, head_dim]: q[b,h,d] at q + b*q_stride_b + h*q_stride_h + d.
+ * q        [batch, q_len, n_q_heads, head_dim]:
+ *          q[b,i,h,d] at q + b*q_stride_b + i*q_stride_t + h*q_stride_h + d
+ *          (q_len = 1: [batch, n_q_heads, head_dim], q_stride_t unused).
  * Contiguous cache (page_size == 0): key j of (b, KV head g) at
  *          k_cache + b*k_stride_b + g*k_stride_h + j*k_stride_t, j < kv_extent
  *          (e.g. a dense [batch, n_kv_heads, T_max, head_dim] tensor: kv_extent = T_max).
@@ -110,7 +123,8 @@ typedef struct fd_desc {
     int32_t max_seqlen;         /* host-known upper bound of seqlens[]; used when n_splits <= 0 */
     int32_t n_splits;           /* >= 1: use it; <= 0: plan it with fd_plan's rule from max_seqlen */
     int32_t flags;              /* 0, or FD_FLAG_* bits */
-    int32_t reserved;           /* must be 0 */
+    int32_t q_len;              /* query positions per sequence; 0 or 1 = one (plain decode) */
+    int64_t q_stride_t;         /* elements between query positions (q_len > 1) */
 } fd_desc;
 
 /* ABI version of the loaded library (FD_ABI_VERSION at build time). */
@@ -134,22 +148,26 @@ int32_t fd_num_sms(int32_t device);
 int32_t fd_plan_splits(int64_t work_items, int64_t slots, int64_t n_kv_blocks,
                        int32_t max_splits);
 
-/* n_splits for one decode step: fd_plan_splits(batch*n_kv_heads, 2*num_sms,
+/* n_splits for one decode step with one query position per sequence:
+ * fd_plan_splits(batch*n_kv_heads, 2*num_sms,
  * ceil(max_b seqlens_host[b] / 128), 128).  work is KV heads x batch because a
  * CTA serves a whole GQA group ("Flash-Decoding ...", §1 GQA note); two slots
  * per SM as in the page's §6 dispatcher.  seqlens_host: host array of `batch`
  * lengths (>= 0).  num_sms <= 0 queries the current device.  The result
  * depends only on batch, n_kv_heads, max seqlen and num_sms; n_q_heads and
- * head_dim are validated only.  Returns s in [1, 128] or a negative fd_status. */
+ * head_dim are validated only.  Returns s in [1, 128] or a negative fd_status.
+ * (fd_decode, given n_splits <= 0, plans query blocks the same way with
+ * work = batch*n_kv_heads*ceil(G*q_len/16), the CTAs per split.) */
 int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                 const int32_t* seqlens_host, int32_t num_sms);
 
 /* Bytes of workspace fd_decode needs for `n_splits` (<= 0: the split count
  * fd_decode would plan).  Layout (all fp32, each section 256-byte aligned,
- * row r = b*n_q_heads + h):
- *     u  [batch*n_q_heads][n_splits][head_dim]   unnormalised partial outputs
- *     m  [batch*n_q_heads][n_splits]             max score of the split (natural units of s)
- *     l  [batch*n_q_heads][n_splits]             sum of exp(s - m) over the split
+ * row r = (b*q_len + i)*n_q_heads + h):
+ *     u  [rows][n_splits][head_dim]   unnormalised partial outputs
+ *     m  [rows][n_splits]             max score of the split (natural units of s)
+ *     l  [rows][n_splits]             sum of exp(s - m) over the split
+ * with rows = batch*q_len*n_q_heads.
  * An empty split holds u = 0, m = -inf, l = 0.  Returns 0 for an invalid
  * descriptor. */
 size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits);
@@ -160,8 +178,8 @@ size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits);
  *                        capacity = kv_extent (contiguous) or
  *                        max_pages_per_seq*page_size (paged).
  *  block_table         : device int32[batch*max_pages_per_seq] (paged), else NULL.
- *  out                 : device [batch, n_q_heads, head_dim], out_dtype, contiguous.
- *  lse                 : device float[batch*n_q_heads], natural-log LSE of the
+ *  out                 : device [batch, q_len, n_q_heads, head_dim], out_dtype, contiguous.
+ *  lse                 : device float[batch*q_len*n_q_heads], natural-log LSE of the
  *                        scaled scores; NULL to skip.  A row with seqlens[b] = 0
  *                        gets out = 0 and lse = -inf.
  *  workspace           : device, >= fd_workspace_size(desc, n_splits) bytes,

@@ -60,7 +60,8 @@ class FdDesc(ctypes.Structure):
         ("kv_extent", ctypes.c_int64),
         ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
         ("max_seqlen", ctypes.c_int32), ("n_splits", ctypes.c_int32),
-        ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32), ("q_len", ctypes.c_int32),
+        ("q_stride_t", ctypes.c_int64),
     ]
 
     def copy(self) -> "FdDesc":
@@ -219,17 +220,26 @@ def _dtype_code(t) -> int:
 def make_desc(q, k_cache, v_cache, *, n_kv_heads: int | None = None, page_size: int = 0,
               max_pages_per_seq: int = 0, max_seqlen: int = 0, n_splits: int = 0,
               out_dtype=None) -> FdDesc:
-    """Descriptor for q [B, Hq, D] and a cache given as 4-D strided tensors:
-    contiguous [B, Hkv, T, D] (page_size 0) or a paged pool [P, Hkv, page, D]
-    (any strided view of that shape, e.g. a permuted [P, page, Hkv, D])."""
+    """Descriptor for q [B, Hq, D] (or a query block [B, q_len, Hq, D]) and a
+    cache given as 4-D strided tensors: contiguous [B, Hkv, T, D] (page_size 0)
+    or a paged pool [P, Hkv, page, D] (any strided view of that shape, e.g. a
+    permuted [P, page, Hkv, D])."""
     import torch
-    B, Hq, D = q.shape
     d = FdDesc()
+    if q.dim() == 4:
+        B, q_len, Hq, D = q.shape
+        d.q_len = q_len
+        d.q_stride_t = q.stride(1)
+        d.q_stride_b, d.q_stride_h = q.stride(0), q.stride(2)
+    else:
+        B, Hq, D = q.shape
+        d.q_len = 1
+        d.q_stride_t = 0
+        d.q_stride_b, d.q_stride_h = q.stride(0), q.stride(1)
     d.batch, d.n_q_heads, d.head_dim = B, Hq, D
     d.n_kv_heads = int(n_kv_heads if n_kv_heads is not None else k_cache.shape[1])
     d.kv_dtype = _dtype_code(k_cache.dtype)
     d.out_dtype = _dtype_code(out_dtype if out_dtype is not None else torch.float32)
-    d.q_stride_b, d.q_stride_h = q.stride(0), q.stride(1)
     d.k_stride_b, d.k_stride_h, d.k_stride_t = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
     d.v_stride_b, d.v_stride_h, d.v_stride_t = v_cache.stride(0), v_cache.stride(1), v_cache.stride(2)
     if page_size:
@@ -243,5 +253,4 @@ def make_desc(q, k_cache, v_cache, *, n_kv_heads: int | None = None, page_size: 
     d.max_seqlen = int(max_seqlen)
     d.n_splits = int(n_splits)
     d.flags = 0
-    d.reserved = 0
     return d

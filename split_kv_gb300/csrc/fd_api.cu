@@ -37,12 +37,23 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool stride_ok(int64_t s) { return s >= 0 && s % 8 == 0 && s < (int64_t(1) << 38); }
 
+int q_len_of(const fd_desc* d) { return d->q_len <= 1 ? 1 : d->q_len; }
+
+int64_t rows_of(const fd_desc* d) {
+    return static_cast<int64_t>(d->batch) * q_len_of(d) * d->n_q_heads;
+}
+
+int col_blocks_of(const fd_desc* d) {
+    return fdk::column_blocks((d->n_q_heads / d->n_kv_heads) * q_len_of(d));
+}
+
 // Shape / layout checks shared by every entry point.  Pointer checks are
 // done by the callers, which know which pointers they use.
 fd_status check_desc(const fd_desc* d) {
     if (d == nullptr) return FD_ERR_INVALID_ARG;
-    if ((d->flags & ~(FD_FLAG_CUDA_CORES | FD_FLAG_TEST_DROP_FIRST_STAGE)) != 0 || d->reserved != 0)
+    if ((d->flags & ~(FD_FLAG_CUDA_CORES | FD_FLAG_TEST_DROP_FIRST_STAGE)) != 0)
         return FD_ERR_INVALID_ARG;
+    if (d->q_len < 0) return FD_ERR_INVALID_ARG;
     if (d->batch < 0 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1)
         return FD_ERR_INVALID_ARG;
     if (d->n_q_heads % d->n_kv_heads != 0) return FD_ERR_INVALID_ARG;
@@ -52,7 +63,11 @@ fd_status check_desc(const fd_desc* d) {
         return FD_ERR_INVALID_ARG;
     if (d->head_dim != kHeadDim) return FD_ERR_UNSUPPORTED;
     const int G = d->n_q_heads / d->n_kv_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return FD_ERR_UNSUPPORTED;
+    const int ql = q_len_of(d);
+    if (ql > 16 || static_cast<int64_t>(G) * ql > 256) return FD_ERR_UNSUPPORTED;
+    if ((d->flags & FD_FLAG_CUDA_CORES) != 0 && ((G != 1 && G != 2 && G != 4 && G != 8) || ql != 1))
+        return FD_ERR_UNSUPPORTED;
+    if (ql > 1 && !stride_ok(d->q_stride_t)) return FD_ERR_INVALID_ARG;
     if (d->n_splits > FD_MAX_SPLITS) return FD_ERR_UNSUPPORTED;
     if (d->page_size < 0) return FD_ERR_INVALID_ARG;
     if (d->page_size > 0) {
@@ -80,8 +95,8 @@ int32_t splits_for(const fd_desc* d) {
     const int32_t sms = fd_num_sms(-1);
     if (sms < 0) return sms;
     const int64_t blocks = (static_cast<int64_t>(d->max_seqlen) + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS;
-    return fd_plan_splits(static_cast<int64_t>(d->batch) * d->n_kv_heads, 2 * static_cast<int64_t>(sms),
-                          blocks, FD_MAX_SPLITS);
+    return fd_plan_splits(static_cast<int64_t>(d->batch) * d->n_kv_heads * col_blocks_of(d),
+                          2 * static_cast<int64_t>(sms), blocks, FD_MAX_SPLITS);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -138,12 +153,13 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FD_ERR_INVALID_ARG;
     const bool paged = d->page_size > 0;
     if (paged != (block_table != nullptr)) return FD_ERR_INVALID_ARG;
-    const int64_t rows = static_cast<int64_t>(d->batch) * d->n_q_heads;
+    const int64_t rows = rows_of(d);
     const WsLayout w = ws_layout(rows, S);
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FD_ERR_WORKSPACE;
     if (workspace_bytes < w.total) return FD_ERR_WORKSPACE;
     if (d->batch == 0) return FD_OK;
-    if (d->batch > 65535 || d->n_kv_heads > 65535) return FD_ERR_UNSUPPORTED;
+    if (d->batch > 65535 || static_cast<int64_t>(d->n_kv_heads) * col_blocks_of(d) > 65535)
+        return FD_ERR_UNSUPPORTED;
 
     CUtensorMap tmK, tmV;
     fd_status st = make_map(&tmK, d, k, d->k_stride_b, d->k_stride_h, d->k_stride_t);
@@ -155,6 +171,11 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.q = q;
     p.q_sb = d->q_stride_b;
     p.q_sh = d->q_stride_h;
+    p.q_st = q_len_of(d) > 1 ? d->q_stride_t : 0;
+    p.group = d->n_q_heads / d->n_kv_heads;
+    p.q_len = q_len_of(d);
+    p.cols = p.group * p.q_len;
+    p.col_blocks = col_blocks_of(d);
     p.seqlens = seqlens;
     p.block_table = block_table;
     p.max_pages = paged ? d->max_pages_per_seq : 0;
@@ -175,7 +196,7 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);
     p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
     p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
-    const cudaError_t e = fdk::launch_split(tmK, tmV, p, d->kv_dtype, d->n_q_heads / d->n_kv_heads,
+    const cudaError_t e = fdk::launch_split(tmK, tmV, p, d->kv_dtype,
                                             (d->flags & FD_FLAG_CUDA_CORES) != 0, d->batch,
                                             d->n_kv_heads, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
@@ -184,7 +205,7 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
 fd_status combine_impl(const fd_desc* d, int32_t S, const void* workspace, size_t workspace_bytes,
                        void* out, float* lse, cudaStream_t stream) {
     if (workspace == nullptr || out == nullptr) return FD_ERR_INVALID_ARG;
-    const int64_t rows = static_cast<int64_t>(d->batch) * d->n_q_heads;
+    const int64_t rows = rows_of(d);
     const WsLayout w = ws_layout(rows, S);
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FD_ERR_WORKSPACE;
     if (workspace_bytes < w.total) return FD_ERR_WORKSPACE;
@@ -255,7 +276,7 @@ size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits) {
     int32_t S = n_splits;
     if (S <= 0) S = splits_for(desc);
     if (S < 1 || S > FD_MAX_SPLITS) return 0;
-    return ws_layout(static_cast<int64_t>(desc->batch) * desc->n_q_heads, S).total;
+    return ws_layout(rows_of(desc), S).total;
 }
 
 fd_status fd_split_states(const fd_desc* desc, const void* q, const void* k_cache,
@@ -300,7 +321,7 @@ fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cac
     if (out == nullptr) return FD_ERR_INVALID_ARG;
     const int32_t S = splits_for(desc);
     if (S < 1) return static_cast<fd_status>(S < 0 ? S : FD_ERR_INVALID_ARG);
-    const size_t need = ws_layout(static_cast<int64_t>(desc->batch) * desc->n_q_heads, S).total;
+    const size_t need = ws_layout(rows_of(desc), S).total;
     if (need > FD_STATIC_WORKSPACE_BYTES) return FD_ERR_WORKSPACE;
     void* ws = nullptr;
     st = static_workspace(&ws);

@@ -25,7 +25,7 @@ constexpr unsigned kStatusPageBit = 4u;      // block-table entry outside [0, n_
 
 struct SplitParams {
     const void* q;
-    int64_t q_sb, q_sh;             // elements
+    int64_t q_sb, q_sh, q_st;       // elements: sequence, head, query position
     const int32_t* seqlens;
     const int32_t* block_table;     // paged only
     int32_t max_pages;              // block_table row length
@@ -34,6 +34,10 @@ struct SplitParams {
     int32_t capacity;               // tokens a sequence may hold
     int32_t n_pages;                // paged pool size
     int32_t n_q_heads;
+    int32_t group;                  // G = query heads per KV head
+    int32_t q_len;                  // query positions per sequence
+    int32_t cols;                   // G * q_len (query position, head) columns per KV head
+    int32_t col_blocks;             // CTAs per (split, KV head): ceil(cols / 16), 1 if cols <= 8
     int32_t n_splits;
     int32_t split_unit;             // split ranges are whole units of this many tokens
     int32_t drop_first_stage;       // test hook: never request stage 0 (the wait for it times out)
@@ -80,8 +84,11 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
 // Launchers return cudaGetLastError() after the launch.
 // cuda_cores selects the CUDA-core (FP32 FMA) consumer instead of the tensor-core one.
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, int group, bool cuda_cores, int batch, int n_kv_heads,
+                         int kv_dtype, bool cuda_cores, int batch, int n_kv_heads,
                          cudaStream_t stream);
+
+// CTAs per (split, KV head) for G * q_len columns.
+inline int column_blocks(int cols) { return cols <= 8 ? 1 : (cols + 15) / 16; }
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Device status word helpers (fd_split.cu owns the symbol).

@@ -138,10 +138,11 @@ constexpr int kOffAlpha = kOffP + kConsumerWarps * 16 * 8 * 4;    // [warps][8] 
 constexpr int kOffFlag = kOffAlpha + kConsumerWarps * 8 * 4;      // abort flag
 constexpr int kSmemUsed = kOffFlag + 16;
 // end-of-split merge area (reuses stage memory once every stage is consumed)
-constexpr int kOffWAcc = 0;                                       // [warps][8][128] f32
-constexpr int kOffWM = kConsumerWarps * 8 * kHeadDim * 4;         // [warps][8]
-constexpr int kOffWL = kOffWM + kConsumerWarps * 8 * 4;           // [warps][8]
-static_assert(kOffWL + kConsumerWarps * 8 * 4 <= kOffBars, "merge area must fit in the stages");
+constexpr int kCols = 16;                                         // (query, head) columns per CTA
+constexpr int kOffWAcc = 0;                                       // [warps][16][128] f32
+constexpr int kOffWM = kConsumerWarps * kCols * kHeadDim * 4;     // [warps][16]
+constexpr int kOffWL = kOffWM + kConsumerWarps * kCols * 4;       // [warps][16]
+static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
 
 }  // namespace
 
@@ -155,6 +156,8 @@ struct SplitCtx {
     volatile int* abort_flag;   // any warp gave up
     volatile int* cons_abort;   // a consumer warp gave up
     int b, kvh, split;
+    int cb;                     // block of 16 (query, head) columns this CTA serves
+    int L;                      // the sequence's length (keys in the cache)
     int tok0, tok1, n_sub;
 
     __device__ __forceinline__ uint32_t full_bar(int s) const { return bar0 + 8u * s; }
@@ -370,28 +373,31 @@ __device__ __forceinline__ bool consume_simt(const SplitCtx& c, int cw, int lane
     float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
     float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
     if (owner && hw == 0) {
-        wm[cw * 8 + g_lane] = m_run;
-        wl[cw * 8 + g_lane] = l_run;
+        wm[cw * kCols + g_lane] = m_run;
+        wl[cw * kCols + g_lane] = l_run;
     }
 #pragma unroll
     for (int g = 0; g < G; ++g)
-        *reinterpret_cast<float4*>(wacc + (cw * 8 + g) * kHeadDim + 4 * lane) =
+        *reinterpret_cast<float4*>(wacc + (cw * kCols + g) * kHeadDim + 4 * lane) =
             make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
     return true;
 }
 
 // ---------------------------------------------------------------------------
 // Consumer, tensor-core path: the packed group's QK^T and PV on warp-level
-// MMAs (m16n8k16, f32 accumulate), "swap-AB" so that 16 tokens are the M
-// rows and the group's <= 8 query heads the N columns:
-//   S^T[16 tok x 8 heads]  = K[16 tok x 128]   . Q^T[128 x 8]     (8 MMAs)
-//   O^T[128 dims x 8 heads] += V^T[128 x 16 tok] . P^T[16 tok x 8]  (8 x 2 MMAs)
+// MMAs (m16n8k16, f32 accumulate), "swap-AB": 16 tokens are the M rows and up
+// to 8 * NB (query position, head) columns of the group are N:
+//   S^T[16 tok x 8]  = K[16 tok x 128]   . Q^T[128 x 8]        (8 MMAs per N block)
+//   O^T[128 x 8]    += V^T[128 x 16 tok] . P^T[16 tok x 8]     (8 x 2 MMAs per N block)
+// Column n of the CTA's block cb is query position i = (16 cb + n) / G and
+// head g = (16 cb + n) % G of the group; it sees the first L - q_len + 1 + i
+// keys.  One query per sequence (q_len = 1) is the plain decode step.
 // K and V^T fragments come straight from the swizzled stage with ldmatrix
 // (no conversion instructions); P^T is the transposed S^T accumulator
 // (movmatrix), carried as hi + lo 16-bit parts so that PV keeps ~2^-18
 // relative precision in P even for bf16.
-// Lane (gid = lane/4, tig = lane%4) holds heads 2tig, 2tig+1 of tokens gid,
-// gid+8 in S^T and dims 16mb+gid(+8) of the same two heads in O^T.
+// Lane (gid = lane/4, tig = lane%4) holds columns 8j + 2tig, 8j + 2tig + 1 of
+// tokens gid, gid+8 in S^T and dims 16mb+gid(+8) of the same columns in O^T.
 // ---------------------------------------------------------------------------
 template <typename T>
 struct Mma;
@@ -460,36 +466,53 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <typename T, int G>
+template <typename T, int NB>
 __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) {
-    static_assert(G <= 8, "the MMA N dimension holds at most 8 heads");
     const SplitParams& p = *c.p;
     const int gid = lane >> 2, tig = lane & 3;
-    const int h0 = 2 * tig, h1 = 2 * tig + 1;    // this lane's two heads (>= G: padding)
     const int r0 = cw * 16;                      // the warp's 16 rows of each stage
+    const int G = p.group;
 
-    // Q^T as the B operand: b0 = q[gid][16kb + 2tig .. +1], b1 = q[gid][16kb + 8 + 2tig .. +1]
-    uint32_t qb[8][2];
-    {
-        const bool real = gid < G;
+    // Q^T as the B operand of N block j: column 8j + gid,
+    // b0 = q[.][16kb + 2tig .. +1], b1 = q[.][16kb + 8 + 2tig .. +1]
+    uint32_t qb[NB][8][2];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        const int n = c.cb * kCols + 8 * j + gid;
+        const bool real = n < p.cols;
+        const int i = real ? n / G : 0, g = real ? n % G : 0;
         const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(c.b) * p.q_sb +
-                        static_cast<int64_t>(c.kvh * G + (real ? gid : 0)) * p.q_sh;
+                        static_cast<int64_t>(i) * p.q_st +
+                        static_cast<int64_t>(c.kvh * G + g) * p.q_sh;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             const uint32_t lo = __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kb + 2 * tig));
             const uint32_t hi = __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kb + 8 + 2 * tig));
-            qb[kb][0] = real ? lo : 0u;
-            qb[kb][1] = real ? hi : 0u;
+            qb[j][kb][0] = real ? lo : 0u;
+            qb[j][kb][1] = real ? hi : 0u;
         }
     }
+    // keys visible to this lane's columns: the first L - q_len + 1 + i
+    int vis[NB][2];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = c.cb * kCols + 8 * j + 2 * tig + e;
+            vis[j][e] = n < p.cols ? c.L - p.q_len + 1 + n / G : c.L;
+        }
 
-    float m0 = -INFINITY, m1 = -INFINITY;   // base-2 running max of heads h0, h1
-    float l0 = 0.f, l1 = 0.f;               // this lane's share of the running sums
-    float acc[8][4];
+    float m[NB][2], l[NB][2];               // base-2 running max; this lane's share of the sums
+    float acc[8][NB][4];
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb)
+    for (int j = 0; j < NB; ++j) {
+        m[j][0] = m[j][1] = -INFINITY;
+        l[j][0] = l[j][1] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[mb][j] = 0.f;
+        for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mb][j][e] = 0.f;
+    }
 
     // ldmatrix row addresses (bytes within a half box, before the stage base)
     // K (A operand, not transposed): matrix j = lane/8 holds tokens +0/+8 and dims +0/+8
@@ -500,16 +523,17 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
     const int v_csel = (lane >> 3) & 1;
 
 #pragma unroll 1
-    for (int i = 0; i < c.n_sub; ++i) {
-        const int st = i % kStages;
-        const bool ok = wait_or_flag(c.full_bar(st), (i / kStages) & 1);
+    for (int it = 0; it < c.n_sub; ++it) {
+        const int st = it % kStages;
+        const bool ok = wait_or_flag(c.full_bar(st), (it / kStages) & 1);
         if (!__all_sync(kFull, ok)) {
             *c.cons_abort = 1;
             *c.abort_flag = 1;
             break;
         }
         uint8_t* sb = c.smem + st * kStageBytes;
-        const int nvalid = min(kSub, c.tok1 - (c.tok0 + i * kSub));
+        const int stage_tok = c.tok0 + it * kSub;
+        const int nvalid = min(kSub, c.tok1 - stage_tok);
 
         // Rows past the sequence end hold whatever the cache holds there; P is
         // 0 for them, but 0 * NaN would still poison PV, so zero those V rows.
@@ -528,7 +552,9 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         }
 
         // ---- S^T = K . Q^T for the warp's 16 tokens
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        float s[NB][4];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
         const uint32_t kbase = smem_u32(sb);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
@@ -537,51 +563,62 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
                                   (((chunk & 7) ^ (k_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4(a, addr);
-            Mma<T>::run(s, a, qb[kb][0], qb[kb][1]);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) Mma<T>::run(s[j], a, qb[j][kb][0], qb[j][kb][1]);
         }
 
-        // ---- online softmax (base 2) for heads h0, h1 over the 16 tokens
-        const bool v0 = r0 + gid < nvalid, v1 = r0 + gid + 8 < nvalid;
+        // ---- online softmax (base 2) per column over the 16 tokens
         const float sc = p.score_scale_log2;
-        const float t0 = v0 ? s[0] * sc : -INFINITY;   // token gid,   head h0
-        const float t1 = v0 ? s[1] * sc : -INFINITY;   // token gid,   head h1
-        const float t2 = v1 ? s[2] * sc : -INFINITY;   // token gid+8, head h0
-        const float t3 = v1 ? s[3] * sc : -INFINITY;   // token gid+8, head h1
-        float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+        const int row0 = r0 + gid, row1 = r0 + gid + 8;    // rows in the stage
+        bool rescale = false;
+        uint32_t bh[NB][2], bl[NB][2];
+        float al[NB][2];
 #pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-        }
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float u0 = n0 == -INFINITY ? 0.f : n0;   // never -inf - -inf
-        const float u1 = n1 == -INFINITY ? 0.f : n1;
-        const float a0 = fast_exp2(m0 - u0), a1 = fast_exp2(m1 - u1);
-        const float p0 = fast_exp2(t0 - u0), p1 = fast_exp2(t1 - u1);
-        const float p2 = fast_exp2(t2 - u0), p3 = fast_exp2(t3 - u1);
-        l0 = fmaf(a0, l0, p0 + p2);
-        l1 = fmaf(a1, l1, p1 + p3);
-        m0 = n0;
-        m1 = n1;
-        if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
+        for (int j = 0; j < NB; ++j) {
+            float t[4];
 #pragma unroll
-            for (int mb = 0; mb < 8; ++mb) {
-                acc[mb][0] *= a0;
-                acc[mb][1] *= a1;
-                acc[mb][2] *= a0;
-                acc[mb][3] *= a1;
+            for (int e = 0; e < 2; ++e) {
+                const int lim = min(nvalid, vis[j][e] - stage_tok);
+                t[e] = row0 < lim ? s[j][e] * sc : -INFINITY;         // token gid
+                t[e + 2] = row1 < lim ? s[j][e + 2] * sc : -INFINITY; // token gid + 8
             }
+            float pr[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(t[e], t[e + 2]);
+#pragma unroll
+                for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+                const float mn = fmaxf(m[j][e], mx);
+                const float mu = mn == -INFINITY ? 0.f : mn;   // never -inf - -inf
+                al[j][e] = fast_exp2(m[j][e] - mu);
+                pr[e] = fast_exp2(t[e] - mu);
+                pr[e + 2] = fast_exp2(t[e + 2] - mu);
+                l[j][e] = fmaf(al[j][e], l[j][e], pr[e] + pr[e + 2]);
+                m[j][e] = mn;
+                rescale |= al[j][e] != 1.f;
+            }
+            // P^T as B fragments: hi + lo parts, transposed in registers
+            float k0, k1, k2, k3, d0, d1, d2, d3;
+            const uint32_t hi01 = Mma<T>::pack(pr[0], pr[1], k0, k1);
+            const uint32_t hi23 = Mma<T>::pack(pr[2], pr[3], k2, k3);
+            const uint32_t lo01 = Mma<T>::pack(pr[0] - k0, pr[1] - k1, d0, d1);
+            const uint32_t lo23 = Mma<T>::pack(pr[2] - k2, pr[3] - k3, d2, d3);
+            bh[j][0] = movmatrix_trans(hi01);
+            bh[j][1] = movmatrix_trans(hi23);
+            bl[j][0] = movmatrix_trans(lo01);
+            bl[j][1] = movmatrix_trans(lo23);
         }
-
-        // ---- P^T as B fragments: hi + lo parts, transposed in registers
-        float k0, k1, k2, k3;
-        const uint32_t hi01 = Mma<T>::pack(p0, p1, k0, k1);
-        const uint32_t hi23 = Mma<T>::pack(p2, p3, k2, k3);
-        float d0, d1, d2, d3;
-        const uint32_t lo01 = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
-        const uint32_t lo23 = Mma<T>::pack(p2 - k2, p3 - k3, d2, d3);
-        const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
-        const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+        if (__any_sync(kFull, rescale)) {
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    acc[mb][j][0] *= al[j][0];
+                    acc[mb][j][1] *= al[j][1];
+                    acc[mb][j][2] *= al[j][0];
+                    acc[mb][j][3] *= al[j][1];
+                }
+        }
 
         // ---- O^T += V^T . P^T
         const uint32_t vbase = smem_u32(sb + 2 * kHalfBytes);
@@ -592,55 +629,75 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
                                   (((chunk & 7) ^ (v_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4_trans(a, addr);
-            Mma<T>::run(acc[mb], a, bh0, bh1);
-            Mma<T>::run(acc[mb], a, bl0, bl1);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                Mma<T>::run(acc[mb][j], a, bh[j][0], bh[j][1]);
+                Mma<T>::run(acc[mb][j], a, bl[j][0], bl[j][1]);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(c.empty_bar(st));
     }
 
-    // lane sums -> head sums over the 8 token rows (lanes with equal tig)
+    // lane sums -> column sums over the 8 token rows (lanes with equal tig)
 #pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, o);
-        l1 += __shfl_xor_sync(kFull, l1, o);
-    }
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) l[j][e] += __shfl_xor_sync(kFull, l[j][e], o);
 
     named_sync(1, kConsumerWarps * 32);
     if (*c.cons_abort) return false;   // states are not written after a timeout
     float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
     float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
     float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
-    if (gid == 0) {
-        if (h0 < G) {
-            wm[cw * 8 + h0] = m0;
-            wl[cw * 8 + h0] = l0;
-        }
-        if (h1 < G) {
-            wm[cw * 8 + h1] = m1;
-            wl[cw * 8 + h1] = l1;
-        }
-    }
 #pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-        const int d = 16 * mb + gid;
-        if (h0 < G) {
-            wacc[(cw * 8 + h0) * kHeadDim + d] = acc[mb][0];
-            wacc[(cw * 8 + h0) * kHeadDim + d + 8] = acc[mb][2];
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int col = 8 * j + 2 * tig + e;
+            if (gid == 0) {
+                wm[cw * kCols + col] = m[j][e];
+                wl[cw * kCols + col] = l[j][e];
+            }
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb) {
+                wacc[(cw * kCols + col) * kHeadDim + 16 * mb + gid] = acc[mb][j][e];
+                wacc[(cw * kCols + col) * kHeadDim + 16 * mb + gid + 8] = acc[mb][j][e + 2];
+            }
         }
-        if (h1 < G) {
-            wacc[(cw * 8 + h1) * kHeadDim + d] = acc[mb][1];
-            wacc[(cw * 8 + h1) * kHeadDim + d + 8] = acc[mb][3];
-        }
-    }
     return true;
 }
 
 // ---------------------------------------------------------------------------
-// The split kernel.  TC selects the tensor-core consumer (default) or the
-// CUDA-core one; both leave the same per-warp states for the final merge.
+// The split kernel.  CONSUME is consume_tc<T, NB> (default) or
+// consume_simt<T, G>; both leave per-warp states of up to 16 columns for the
+// final merge.
 // ---------------------------------------------------------------------------
-template <typename T, int G, bool TC>
+template <typename T, int KIND>
+struct Consumer;
+// KIND 1, 2: tensor cores with 8 or 16 columns; KIND 10 + G: CUDA cores, group G
+template <typename T> struct Consumer<T, 1> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 2> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 11> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 1>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 12> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 2>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 14> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 4>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 18> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 8>(c, w, l); }
+};
+
+template <typename T, int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
@@ -652,7 +709,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     c.p = &p;
     c.smem = smem;
     c.split = blockIdx.x;
-    c.kvh = blockIdx.y;
+    c.kvh = blockIdx.y / p.col_blocks;
+    c.cb = blockIdx.y % p.col_blocks;
     c.b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -686,9 +744,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     // a page and a paged cache splits exactly like a contiguous one
     int L = __ldg(p.seqlens + c.b);
     if (L < 0 || L > p.capacity) {
-        if (threadIdx.x == 0 && c.split == 0 && c.kvh == 0) raise_status(kStatusSeqlenBit);
+        if (threadIdx.x == 0 && c.split == 0 && blockIdx.y == 0) raise_status(kStatusSeqlenBit);
         L = L < 0 ? 0 : p.capacity;
     }
+    c.L = L;
     const int unit = p.split_unit;
     const int n_units = (L + unit - 1) / unit;
     const int base = n_units / S, rem = n_units % S;
@@ -704,36 +763,34 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     }
 
-    bool ok;
-    if constexpr (TC)
-        ok = consume_tc<T, G>(c, warp, lane);
-    else
-        ok = consume_simt<T, G>(c, warp, lane);
-    if (!ok) return;
+    if (!Consumer<T, KIND>::run(c, warp, lane)) return;
     named_sync(1, kConsumerWarps * 32);
 
-    // ---- merge the four warp states of each head and write the split's state
+    // ---- merge the four warp states of each column and write the split's state
     const float* wacc = reinterpret_cast<const float*>(smem + kOffWAcc);
     const float* wm = reinterpret_cast<const float*>(smem + kOffWM);
     const float* wl = reinterpret_cast<const float*>(smem + kOffWL);
     const int d = threadIdx.x;   // 0 .. 127
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
+    const int ncols = min(kCols, p.cols - c.cb * kCols);
+    for (int col = 0; col < ncols; ++col) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * 8 + g]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * kCols + col]);
         float u = 0.f, l = 0.f, m_out = -INFINITY;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float mw = wm[w * 8 + g];
+                const float mw = wm[w * kCols + col];
                 const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                u = fmaf(e, wacc[(w * 8 + g) * kHeadDim + d], u);
-                l = fmaf(e, wl[w * 8 + g], l);
+                u = fmaf(e, wacc[(w * kCols + col) * kHeadDim + d], u);
+                l = fmaf(e, wl[w * kCols + col], l);
             }
             m_out = M * kLn2;
         }
-        const int64_t row = static_cast<int64_t>(c.b) * p.n_q_heads + c.kvh * G + g;
+        const int n = c.cb * kCols + col;
+        const int i = n / p.group, g = n % p.group;
+        const int64_t row = (static_cast<int64_t>(c.b) * p.q_len + i) * p.n_q_heads +
+                            c.kvh * p.group + g;
         const int64_t idx = row * S + c.split;
         p.ws_u[idx * kHeadDim + d] = u;
         if (d == 0) {
@@ -743,11 +800,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <typename T, int G, bool TC>
+template <typename T, int KIND>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
-    auto kern = fd_split_kernel<T, G, TC>;
+    auto kern = fd_split_kernel<T, KIND>;
     const size_t smem = split_smem_bytes();
     // one attribute call per (kernel, device): cheap and safe to repeat
     static thread_local int configured_device = -1;
@@ -759,33 +816,33 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads, batch), dim3(kThreads), smem, stream,
-                      tmK, tmV, p);
+    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads * p.col_blocks, batch), dim3(kThreads),
+                      smem, stream, tmK, tmV, p);
+}
+
+template <typename T>
+static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                   const SplitParams& p, bool cuda_cores, int batch,
+                                   int n_kv_heads, cudaStream_t stream) {
+    if (cuda_cores) {
+        switch (p.group) {
+            case 1: return launch_split_t<T, 11>(tmK, tmV, p, batch, n_kv_heads, stream);
+            case 2: return launch_split_t<T, 12>(tmK, tmV, p, batch, n_kv_heads, stream);
+            case 4: return launch_split_t<T, 14>(tmK, tmV, p, batch, n_kv_heads, stream);
+            case 8: return launch_split_t<T, 18>(tmK, tmV, p, batch, n_kv_heads, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
+    return p.cols <= 8 ? launch_split_t<T, 1>(tmK, tmV, p, batch, n_kv_heads, stream)
+                       : launch_split_t<T, 2>(tmK, tmV, p, batch, n_kv_heads, stream);
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, int group, bool cuda_cores, int batch, int n_kv_heads,
+                         int kv_dtype, bool cuda_cores, int batch, int n_kv_heads,
                          cudaStream_t stream) {
-#define FD_CASE(TT, GG)                                                                      \
-    return cuda_cores ? launch_split_t<TT, GG, false>(tmK, tmV, p, batch, n_kv_heads, stream) \
-                      : launch_split_t<TT, GG, true>(tmK, tmV, p, batch, n_kv_heads, stream)
-    if (kv_dtype == 0) {
-        switch (group) {
-            case 1: FD_CASE(__half, 1);
-            case 2: FD_CASE(__half, 2);
-            case 4: FD_CASE(__half, 4);
-            case 8: FD_CASE(__half, 8);
-        }
-    } else {
-        switch (group) {
-            case 1: FD_CASE(__nv_bfloat16, 1);
-            case 2: FD_CASE(__nv_bfloat16, 2);
-            case 4: FD_CASE(__nv_bfloat16, 4);
-            case 8: FD_CASE(__nv_bfloat16, 8);
-        }
-    }
-#undef FD_CASE
-    return cudaErrorInvalidValue;
+    if (kv_dtype == 0)
+        return launch_split_dt<__half>(tmK, tmV, p, cuda_cores, batch, n_kv_heads, stream);
+    return launch_split_dt<__nv_bfloat16>(tmK, tmV, p, cuda_cores, batch, n_kv_heads, stream);
 }
 
 cudaError_t read_status(unsigned* value, cudaStream_t stream, bool clear) {

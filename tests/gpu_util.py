@@ -46,9 +46,13 @@ class Guarded:
 
 def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=None,
                n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True, flags=0):
-    """fd_decode through the C ABI; returns (out [B*Hq, D] f64, lse [B*Hq] f64, S)."""
+    """fd_decode through the C ABI; returns (out [rows, D] f64, lse [rows] f64, S)
+    with rows = B*q_len*Hq (q is [B, Hq, D] or a query block [B, q_len, Hq, D])."""
     dev = q.device
-    B, Hq, D = q.shape
+    if q.dim() == 4:
+        B, ql, Hq, D = q.shape
+    else:
+        (B, Hq, D), ql = q.shape, 1
     seqlens_h = np.asarray(seqlens_h, dtype=np.int32)
     seqlens = torch.from_numpy(seqlens_h).to(dev)
     bt = None
@@ -60,13 +64,22 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
                         max_seqlen=int(seqlens_h.max()) if B else 0, n_splits=n_splits,
                         out_dtype=out_dtype)
     desc.flags = flags
-    S = n_splits if n_splits > 0 else fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
+    if n_splits > 0:
+        S = n_splits
+    else:
+        # the planner's rule with the CTAs per split of this query block
+        cols = (Hq // desc.n_kv_heads) * ql
+        cb = 1 if cols <= 8 else -(-cols // 16)
+        S = fd.fd_plan_splits(B * desc.n_kv_heads * cb, 2 * fd.fd_num_sms(),
+                              -(-int(seqlens_h.max()) // 128) if B else 0)
+        if ql == 1:
+            assert S == fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
     assert S >= 1
-    desc.n_splits = S
-    wsb = fd.fd_workspace_size(desc, S)
-    assert wsb > 0
-    out = Guarded(B * Hq * D, out_dtype, dev)
-    lse = Guarded(B * Hq, torch.float32, dev)
+    desc.n_splits = 0 if n_splits <= 0 else S
+    wsb = fd.fd_workspace_size(desc, 0)
+    assert wsb == fd.fd_workspace_size(desc, S) > 0
+    out = Guarded(B * ql * Hq * D, out_dtype, dev)
+    lse = Guarded(B * ql * Hq, torch.float32, dev)
     ws = Guarded(wsb, torch.uint8, dev)
     fd.check(fd.fd_decode(desc, q, k, v, seqlens, bt, out.view, lse.view, ws.view, wsb,
                           stream=stream), "fd_decode")
@@ -76,7 +89,7 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
         assert out.intact(), "fd_decode wrote outside out"
         assert lse.intact(), "fd_decode wrote outside lse"
         assert ws.intact(), "fd_decode wrote outside its workspace"
-    o = out.view.float().cpu().double().numpy().reshape(B * Hq, D)
+    o = out.view.float().cpu().double().numpy().reshape(B * ql * Hq, D)
     l = lse.view.cpu().double().numpy()
     return o, l, S
 

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(fd):
 
 
 def test_abi_version_and_strings(fd):
-    assert fd.fd_abi_version() == 1
+    assert fd.fd_abi_version() == 2
     for code in range(-6, 1):
         s = fd.fd_status_string(code)
         assert s and s != "unknown status"
@@ -45,8 +45,9 @@ def test_abi_version_and_strings(fd):
 
 
 def test_desc_struct_size_matches_header(fd):
-    # 6 int32 + 9 int64 + 6 int32 = 24 + 72 + 24 = 120 bytes, 8-byte aligned
-    assert ctypes.sizeof(fd.FdDesc) == 120
+    # 6 int32 + 9 int64 + 6 int32 + 1 int64 = 24 + 72 + 24 + 8 = 128 bytes
+    assert ctypes.sizeof(fd.FdDesc) == 128
+    assert fd.FdDesc.q_stride_t.offset == 120
 
 
 def test_plan_splits_matches_oracle_table(fd, golden_dir):
@@ -137,7 +138,13 @@ def test_decode_rejects_bad_arguments_without_a_gpu(fd):
         kw.get("bt", None), kw.get("out", fake), kw.get("lse", fake), kw.get("ws", ws),
         kw.get("wsb", big), stream=0)
     assert call(None if False else _desc(fd, head_dim=64)) == fd.FD_ERR_UNSUPPORTED
-    assert call(_desc(fd, n_q_heads=24)) == fd.FD_ERR_UNSUPPORTED           # G = 3
+    cc = fd.FD_FLAG_CUDA_CORES
+    assert call(_desc(fd, n_q_heads=24, flags=cc)) == fd.FD_ERR_UNSUPPORTED  # G = 3 on CUDA cores
+    assert call(_desc(fd, q_len=2, q_stride_t=32 * 128, flags=cc)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, q_len=17, q_stride_t=32 * 128)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, n_q_heads=8 * 40, q_len=8, q_stride_t=320 * 128)) == fd.FD_ERR_UNSUPPORTED
+    assert call(_desc(fd, q_len=-1)) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, q_len=4, q_stride_t=100)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, n_q_heads=20)) == fd.FD_ERR_INVALID_ARG           # 8 does not divide 20
     assert call(_desc(fd, kv_dtype=fd.FD_F32)) == fd.FD_ERR_UNSUPPORTED
     assert call(_desc(fd, kv_dtype=7)) == fd.FD_ERR_INVALID_ARG

@@ -450,3 +450,49 @@ def test_fd_decode_replays_from_a_cuda_graph():
         assert_parity(out.cpu().double().numpy().reshape(B * Hq, D),
                       lse.cpu().double().numpy().reshape(-1), ref_o, ref_l, f"graph replay {seed}")
     assert fd.fd_device_status(clear=True) == fd.FD_OK
+
+
+# ---------------------------------------------------------------- query blocks, any group
+@pytest.mark.parametrize("q_len", [2, 4, 8])
+@pytest.mark.parametrize("group", [1, 3, 4, 8])
+def test_query_blocks(q_len, group):
+    """Short query blocks ("Flash-Decoding ..." §7): position i of a sequence
+    with L keys sees the first L - q_len + 1 + i ([DKV] §06 per-query
+    visibility).  G*q_len ranges from 2 to 64 columns (1 to 4 CTAs per split);
+    the 5-token sequence leaves early positions of an 8-block without keys."""
+    B, Hkv, D, T = 3, 2, 128, 1200
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, q_len, Hq, D), "bf16", 1400 + 10 * q_len + group, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "bf16", 1500 + group)
+    sl = np.array([1200, 130, 5], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "bf16", Hkv)
+    for S in (0, 3, 128):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"q_len={q_len} G={group} S={S}")
+
+
+def test_query_block_paged_and_strided():
+    B, Hkv, G, D, ps, ql = 2, 4, 4, 128, 16, 4
+    lens = [2049, 700]
+    pk, pv, bt = _paged_problem(B, Hkv, D, ps, lens, "f16", 1601)
+    wide = fd_inputs.randn((B, ql, Hkv * G, 2 * D), "f16", 1602, device=DEV)
+    q = wide[..., :D]                                   # strided query block
+    sl = np.array(lens, dtype=np.int32)
+    got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "f16", Hkv, page_size=ps, block_table=bt)
+    assert_parity(got_o, got_l, ref_o, ref_l, "paged query block")
+
+
+@pytest.mark.parametrize("group", [3, 5, 16])
+def test_other_group_sizes_single_query(group):
+    """Groups that are not powers of two, and a 16-wide group, on the
+    tensor-core path (one or two N blocks of the MMA)."""
+    B, Hkv, D, T = 2, 2, 128, 2500
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, Hq, D), "f16", 1700 + group, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "f16", 1710 + group)
+    sl = np.array([2500, 901], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "f16", Hkv)
+    for S in (0, 7):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} S={S}")
