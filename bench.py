@@ -56,7 +56,8 @@ def _args():
     ap.add_argument("--cuda-cores", action="store_true",
                     help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
     ap.add_argument("--workload", default=None,
-                    choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep"],
+                    choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep",
+                             "query_block_q4"],
                     help="time one workload (one JSON line per problem) instead of the default line")
     return ap.parse_args()
 
@@ -543,8 +544,10 @@ def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
         sl_h = fd_inputs.varlen_seqlens(seed, B, T)
     else:
         sl_h = np.full(B, T, dtype=np.int32)
+    q_len = c.get("q_len", 1)
     for j in range(n_sets):
-        q = fd_inputs.randn((B, Hq, D), dt, seed + 100 * j, device=dev)
+        qshape = (B, q_len, Hq, D) if q_len > 1 else (B, Hq, D)
+        q = fd_inputs.randn(qshape, dt, seed + 100 * j, device=dev)
         if name == "paged_b8":
             ps = c["page_size"]
             npp = T // ps
@@ -597,7 +600,13 @@ def run_suite(args):
         sets, sl_h = _problem_sets(name, base, dev, n_sets, batch, ctx)
         seqlens = torch.from_numpy(sl_h).to(dev)
         kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * 2 * 2
-        S_plan = fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
+        ql = c.get("q_len", 1)
+        cols = (c["n_q_heads"] // c["n_kv_heads"]) * ql
+        cblocks = 1 if cols <= 8 else -(-cols // 16)     # CTAs per split (query blocks)
+        S_plan = fd.fd_plan_splits(B * c["n_kv_heads"] * cblocks, 2 * fd.fd_num_sms(),
+                                   -(-int(sl_h.max()) // 128))
+        if ql == 1:
+            assert S_plan == fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
         results = {}
         for label, S in (("planned", S_plan), ("unsplit", 1)):
             if label == "unsplit" and name != "sweep":
@@ -611,8 +620,8 @@ def run_suite(args):
                 descs.append(d)
             wsb = fd.fd_workspace_size(descs[0], S)
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            out = torch.empty(B, c["n_q_heads"], c["head_dim"], dtype=torch.float32, device=dev)
-            lse = torch.empty(B, c["n_q_heads"], dtype=torch.float32, device=dev)
+            out = torch.empty(B, ql, c["n_q_heads"], c["head_dim"], dtype=torch.float32, device=dev)
+            lse = torch.empty(B, ql, c["n_q_heads"], dtype=torch.float32, device=dev)
 
             def call(j, h):
                 _, q, k, v, bt = sets[j]
@@ -625,7 +634,7 @@ def run_suite(args):
             results[label] = (S, ms)
         fd.check(fd.fd_device_status(stream), "device status")
         S, ms = results["planned"]
-        line = {"workload": name, "batch": B, "ctx": T, "n_q_heads": c["n_q_heads"],
+        line = {"workload": name, "batch": B, "ctx": T, "q_len": ql, "n_q_heads": c["n_q_heads"],
                 "n_kv_heads": c["n_kv_heads"], "kv_dtype": c["dtype"], "n_splits": S,
                 "us_per_call": ms * 1e3, "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
                 "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,

@@ -17,6 +17,8 @@ Workloads (the pages measure on no dataset; every input is synthetic):
                  16 tokens, block table a seeded permutation of a shared pool.
   sweep          batch {1,4,16,64} x context {1K,8K,32K,128K,256K}, 32 / 8
                  heads, d=128, fp16.
+  query_block_q4 B=4, 32 / 8 heads, d=128, bf16, 32768 tokens, 4 query
+                 positions per sequence (a speculative-verification block).
 K, V and q are i.i.d. N(0,1) cast to the cache dtype.
 """
 from __future__ import annotations
@@ -36,6 +38,9 @@ WORKLOADS = {
                      dtype="bf16", seed=1004, page_size=16),
     "sweep": dict(batches=(1, 4, 16, 64), ctxs=(1024, 8192, 32768, 131072, 262144),
                   n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="f16", seed=1005),
+    # short query block (speculative verification of 4 draft tokens)
+    "query_block_q4": dict(batch=4, n_q_heads=32, n_kv_heads=8, head_dim=128, ctx=32768,
+                           q_len=4, dtype="bf16", seed=1006),
 }
 
 
