@@ -61,6 +61,8 @@ def _load():
         lib.fdo_half_to_double.argtypes = [ctypes.c_uint16]
         lib.fdo_bf16_to_double.restype = d
         lib.fdo_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.fdo_e4m3_to_double.restype = d
+        lib.fdo_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.fdo_attend.restype = ctypes.c_int
         lib.fdo_attend.argtypes = [i64, ctypes.c_int, vp, vp, vp, d, vp, vp]
         lib.fdo_segment_state.restype = ctypes.c_int
@@ -72,7 +74,7 @@ def _load():
         lib.fdo_plan.restype = ctypes.c_int
         lib.fdo_plan.argtypes = [i64, i64, i64, ctypes.c_int, vp]
         lib.fdo_decode.restype = ctypes.c_int
-        lib.fdo_decode.argtypes = [i32, i32, i32, i32, i32, i32,
+        lib.fdo_decode.argtypes = [i32, i32, i32, i32, i32, i32, d, d, i32,
                                    vp, i64, i64, i64,
                                    vp, i64, i64, i64,
                                    vp, i64, i64, i64,
@@ -104,6 +106,10 @@ def half_to_double(bits: int) -> float:
 
 def bf16_to_double(bits: int) -> float:
     return float(_load().fdo_bf16_to_double(int(bits) & 0xFFFF))
+
+
+def e4m3_to_double(bits: int) -> float:
+    return float(_load().fdo_e4m3_to_double(int(bits) & 0xFF))
 
 
 def attend(q, K, V, scale: float):
@@ -185,8 +191,23 @@ def _bits(a) -> np.ndarray:
     raise TypeError(f"need 16-bit raw patterns, got {a.dtype}")
 
 
+def _bytes8(a) -> np.ndarray:
+    """Raw 8-bit patterns of an fp8 e4m3 cache (numpy uint8 or torch float8/uint8)."""
+    if hasattr(a, "detach"):
+        import torch
+        t = a.detach().contiguous()
+        if t.is_cuda:
+            raise ValueError("oracle inputs must be host arrays")
+        return t.view(torch.uint8).numpy()
+    a = np.asarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError(f"need 8-bit raw patterns, got {a.dtype}")
+    return a
+
+
 def decode(q, k, v, seqlens, *, dtype: str, n_kv_heads: int,
-           page_size: int = 0, block_table=None, rows=None, n_threads: int = 0):
+           page_size: int = 0, block_table=None, rows=None, n_threads: int = 0,
+           kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0):
     """Decode attention in fp64 for every (sequence, query position, query head) row.
 
     q: [B, Hq, D] (one query per sequence) or [B, q_len, Hq, D] (a short query
@@ -194,19 +215,29 @@ def decode(q, k, v, seqlens, *, dtype: str, n_kv_heads: int,
     contiguous k, v: [B, Hkv, T, D] (any 4-D strided
     view whose last dim is contiguous); paged k, v: pool [P, Hkv, page, D] (or
     any 4-D view [P, Hkv, page, D] with contiguous last dim) with block_table
-    [B, max_pages] int32.  dtype: 'f16' or 'bf16'.  rows: optional flat row
-    indices (b*q_len + i)*Hq + h.  Returns (out[n, D] float64, lse[n] float64).
+    [B, max_pages] int32.  dtype: 'f16' or 'bf16', the type of q and (by
+    default) of the cache.  kv_dtype='e4m3': k, v are fp8 E4M3 bytes and key /
+    value j is k_scale / v_scale times the stored value (one scale per tensor).
+    rows: optional flat row indices (b*q_len + i)*Hq + h.  Returns
+    (out[n, D] float64, lse[n] float64).
     """
     dt = {"f16": 0, "bf16": 1}[dtype]
-    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    kvdt = -1 if kv_dtype is None else {"f16": 0, "bf16": 1, "e4m3": 2}[kv_dtype]
+    qb = _bits(q)
+    if kvdt == 2:
+        kb, vb = _bytes8(k), _bytes8(v)
+        esz = 1
+    else:
+        kb, vb = _bits(k), _bits(v)
+        esz = 2
     if qb.ndim == 3:
         qb = qb[:, None]
     B, q_len, Hq, D = qb.shape
-    if qb.strides[-1] != 2 or kb.strides[-1] != 2 or vb.strides[-1] != 2:
+    if qb.strides[-1] != 2 or kb.strides[-1] != esz or vb.strides[-1] != esz:
         raise ValueError("last dim must be contiguous")
     qs = [s // 2 for s in qb.strides]        # b, i, h, d
-    ks = [s // 2 for s in kb.strides]
-    vs = [s // 2 for s in vb.strides]
+    ks = [s // esz for s in kb.strides]
+    vs = [s // esz for s in vb.strides]
     sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
     if sl.shape[0] != B:
         raise ValueError("seqlens must have one entry per sequence")
@@ -223,7 +254,7 @@ def decode(q, k, v, seqlens, *, dtype: str, n_kv_heads: int,
     out = np.empty((n, D))
     lse = np.empty(n)
     rc = _load().fdo_decode(
-        B, Hq, int(n_kv_heads), D, dt, q_len,
+        B, Hq, int(n_kv_heads), D, dt, kvdt, float(k_scale), float(v_scale), q_len,
         qb.ctypes.data, qs[0], qs[1], qs[2],
         kb.ctypes.data, ks[0], ks[1], ks[2],
         vb.ctypes.data, vs[0], vs[1], vs[2],

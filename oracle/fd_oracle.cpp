@@ -79,8 +79,32 @@ double bf16_bits_to_double(uint16_t h) {
     return sign ? -mag : mag;
 }
 
+// OCP FP8 E4M3 ("fn": no infinities): 1 sign bit, 4 exponent bits (bias 7),
+// 3 fraction bits; exponent 15 with fraction 7 is NaN, the rest is finite
+// (largest 448).
+double e4m3_bits_to_double(uint8_t x) {
+    const int sign = (x >> 7) & 1;
+    const int expo = (x >> 3) & 0xf;
+    const int frac = x & 0x7;
+    double mag;
+    if (expo == 0) {
+        mag = std::ldexp(static_cast<double>(frac), -9);            // f/2^3 * 2^-6
+    } else if (expo == 15 && frac == 7) {
+        mag = std::numeric_limits<double>::quiet_NaN();
+    } else {
+        mag = std::ldexp(8.0 + frac, expo - 10);                     // (1 + f/2^3) 2^(e-7)
+    }
+    return sign ? -mag : mag;
+}
+
 double to_double(uint16_t bits, int dtype) {
     return dtype == 0 ? half_bits_to_double(bits) : bf16_bits_to_double(bits);
+}
+
+// Element e of a cache of dtype 0 (fp16), 1 (bf16) or 2 (fp8 e4m3).
+double cache_elem(const void* base, int64_t e, int dtype) {
+    if (dtype == 2) return e4m3_bits_to_double(static_cast<const uint8_t*>(base)[e]);
+    return to_double(static_cast<const uint16_t*>(base)[e], dtype);
 }
 
 // Attention of one query row over L keys, [FD] §1 and §2:
@@ -124,6 +148,7 @@ extern "C" {
 int fdo_abi_version(void) { return 1; }
 
 double fdo_half_to_double(uint16_t bits) { return half_bits_to_double(bits); }
+double fdo_e4m3_to_double(uint8_t bits) { return e4m3_bits_to_double(bits); }
 double fdo_bf16_to_double(uint16_t bits) { return bf16_bits_to_double(bits); }
 
 // Plain attention of one query over L keys in double.  q[D], K[L][D], V[L][D]
@@ -254,14 +279,18 @@ int fdo_plan(int64_t work_items, int64_t slots, int64_t n_kv_blocks, int max_spl
 //    the block table), and the same for v;
 //  * s_j = q.k_j / sqrt(head_dim); out = softmax(s) V, lse = natural-log LSE.
 // q is read at q + b*q_sb + i*q_st + h*q_sh.  dtype 0 = fp16, 1 = bf16 (raw
-// bits).  Rows are numbered r = (b*q_len + i)*n_q_heads + h; rows (nullable)
+// bits) is the type of q and, when kv_dtype < 0, of the cache; kv_dtype 2 is
+// an fp8 e4m3 cache whose key / value j is k_scale / v_scale times the stored
+// value (one scale per tensor; 16-bit caches use the same scales, normally
+// 1).  Strides are in elements of each tensor's own type.
+// Rows are numbered r = (b*q_len + i)*n_q_heads + h; rows (nullable)
 // lists the rows to evaluate, and out/lse then hold n_rows results in that
 // order.  Rows run on n_threads host threads (<= 0: all hardware threads).
 int fdo_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-               int32_t dtype, int32_t q_len,
+               int32_t dtype, int32_t kv_dtype, double k_scale, double v_scale, int32_t q_len,
                const uint16_t* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
-               const uint16_t* k, int64_t k_sb, int64_t k_sh, int64_t k_st,
-               const uint16_t* v, int64_t v_sb, int64_t v_sh, int64_t v_st,
+               const void* k, int64_t k_sb, int64_t k_sh, int64_t k_st,
+               const void* v, int64_t v_sb, int64_t v_sh, int64_t v_st,
                const int32_t* seqlens,
                int32_t page_size, const int32_t* block_table, int32_t max_pages_per_seq,
                const int64_t* rows, int64_t n_rows,
@@ -269,6 +298,8 @@ int fdo_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t hea
     if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || q_len <= 0) return -1;
     if (n_q_heads % n_kv_heads != 0) return -1;
     if (dtype != 0 && dtype != 1) return -1;
+    const int cdt = kv_dtype < 0 ? dtype : kv_dtype;
+    if (cdt != 0 && cdt != 1 && cdt != 2) return -1;
     if (!q || !k || !v || !seqlens || !out || !lse) return -1;
     if (page_size < 0 || (page_size > 0 && (!block_table || max_pages_per_seq <= 0))) return -1;
     const int64_t total = static_cast<int64_t>(batch) * q_len * n_q_heads;
@@ -303,8 +334,8 @@ int fdo_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t hea
                 return P * v_sb + g * v_sh + (j % page_size) * v_st;
             };
             attend_row(L, D, qd.data(),
-                       [&](int64_t j, int d) { return to_double(k[k_off(j) + d], dtype); },
-                       [&](int64_t j, int d) { return to_double(v[v_off(j) + d], dtype); },
+                       [&](int64_t j, int d) { return k_scale * cache_elem(k, k_off(j) + d, cdt); },
+                       [&](int64_t j, int d) { return v_scale * cache_elem(v, v_off(j) + d, cdt); },
                        scale, out + r * D, lse + r, s, acc);
         }
     };

@@ -382,3 +382,44 @@ def test_query_block_against_scipy():
             r = i * Hq + h
             np.testing.assert_allclose(out[r], scipy.special.softmax(s) @ vd[:n], rtol=1e-12, atol=1e-13)
             assert lse[r] == pytest.approx(scipy.special.logsumexp(s), abs=1e-12)
+
+
+# --------------------------------------------------------------------------
+# fp8 e4m3 caches with one scale per tensor
+# --------------------------------------------------------------------------
+def test_e4m3_conversion_all_patterns():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    bits = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = bits.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(int(b)) for b in range(256)])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.nanmax(got) == 448.0
+
+
+def test_e4m3_cache_with_scales_against_scipy():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(91)
+    B, Hq, Hkv, T, D = 2, 4, 2, 40, 16
+    ks, vs = 0.037, 2.5
+    q = rng.standard_normal((B, Hq, D)).astype(np.float16)
+    k8 = torch.from_numpy(rng.standard_normal((B, Hkv, T, D)) * 20).to(torch.float8_e4m3fn)
+    v8 = torch.from_numpy(rng.standard_normal((B, Hkv, T, D))).to(torch.float8_e4m3fn)
+    sl = np.array([40, 13], dtype=np.int32)
+    out, lse = oracle.decode(q, k8, v8, sl, dtype="f16", n_kv_heads=Hkv, kv_dtype="e4m3",
+                             k_scale=ks, v_scale=vs)
+    kd = k8.to(torch.float64).numpy() * ks
+    vd = v8.to(torch.float64).numpy() * vs
+    qd = q.astype(np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            L = sl[b]
+            s = kd[b, h // 2, :L] @ qd[b, h] / math.sqrt(D)
+            np.testing.assert_allclose(out[b * Hq + h], scipy.special.softmax(s) @ vd[b, h // 2, :L],
+                                       rtol=1e-12, atol=1e-13)
+            assert lse[b * Hq + h] == pytest.approx(scipy.special.logsumexp(s), abs=1e-12)
