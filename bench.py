@@ -57,7 +57,7 @@ def _args():
                     help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
     ap.add_argument("--workload", default=None,
                     choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep",
-                             "query_block_q4"],
+                             "query_block_q4", "long_gqa_128k_fp8"],
                     help="time one workload (one JSON line per problem) instead of the default line")
     return ap.parse_args()
 
@@ -556,6 +556,12 @@ def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
             v = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), dt, seed + 100 * j + 2, device=dev)
             bt = torch.from_numpy(fd_inputs.block_table(seed + 2, B, npp, n_pages)).to(dev)
             desc = fd.make_desc(q, k, v, page_size=ps, max_pages_per_seq=npp, max_seqlen=int(sl_h.max()))
+        elif c.get("kv_dtype") == "e4m3":
+            gk = c["kv_gain"]
+            k = fd_inputs.randn_fp8((B, Hkv, T, D), seed + 100 * j + 1, device=dev, gain=gk)
+            v = fd_inputs.randn_fp8((B, Hkv, T, D), seed + 100 * j + 2, device=dev, gain=gk)
+            bt = None
+            desc = fd.make_desc(q, k, v, max_seqlen=int(sl_h.max()), k_scale=1 / gk, v_scale=1 / gk)
         else:
             k = fd_inputs.randn_chunked((B, Hkv, T, D), dt, seed + 100 * j + 1, device=dev)
             v = fd_inputs.randn_chunked((B, Hkv, T, D), dt, seed + 100 * j + 2, device=dev)
@@ -595,11 +601,12 @@ def run_suite(args):
         B = batch or c["batch"]
         T = ctx or c["ctx"]
         per_set = None
-        est = B * c["n_kv_heads"] * T * c["head_dim"] * 4
+        est = B * c["n_kv_heads"] * T * c["head_dim"] * (2 if c.get("kv_dtype") == "e4m3" else 4)
         n_sets = max(1, min(256, _m.ceil(4 * l2 / max(est, 1))))
         sets, sl_h = _problem_sets(name, base, dev, n_sets, batch, ctx)
         seqlens = torch.from_numpy(sl_h).to(dev)
-        kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * 2 * 2
+        esize = 1 if c.get("kv_dtype") == "e4m3" else 2
+        kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * esize * 2
         ql = c.get("q_len", 1)
         cols = (c["n_q_heads"] // c["n_kv_heads"]) * ql
         cblocks = 1 if cols <= 8 else -(-cols // 16)     # CTAs per split (query blocks)
@@ -635,7 +642,7 @@ def run_suite(args):
         fd.check(fd.fd_device_status(stream), "device status")
         S, ms = results["planned"]
         line = {"workload": name, "batch": B, "ctx": T, "q_len": ql, "n_q_heads": c["n_q_heads"],
-                "n_kv_heads": c["n_kv_heads"], "kv_dtype": c["dtype"], "n_splits": S,
+                "n_kv_heads": c["n_kv_heads"], "kv_dtype": c.get("kv_dtype", c["dtype"]), "n_splits": S,
                 "us_per_call": ms * 1e3, "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
                 "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
                 "input_sets": n_sets, "kv_bytes": kv_bytes, "launch": note,

@@ -19,6 +19,8 @@ Workloads (the pages measure on no dataset; every input is synthetic):
                  heads, d=128, fp16.
   query_block_q4 B=4, 32 / 8 heads, d=128, bf16, 32768 tokens, 4 query
                  positions per sequence (a speculative-verification block).
+  long_gqa_128k_fp8  the headline shape with an E4M3 cache (q fp16), values
+                 stored x64 with k_scale = v_scale = 1/64.
 K, V and q are i.i.d. N(0,1) cast to the cache dtype.
 """
 from __future__ import annotations
@@ -38,6 +40,10 @@ WORKLOADS = {
                      dtype="bf16", seed=1004, page_size=16),
     "sweep": dict(batches=(1, 4, 16, 64), ctxs=(1024, 8192, 32768, 131072, 262144),
                   n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="f16", seed=1005),
+    # the headline shape with an fp8 (E4M3) cache, one scale per tensor:
+    # stored = value * kv_gain, k_scale = v_scale = 1 / kv_gain
+    "long_gqa_128k_fp8": dict(batch=1, n_q_heads=32, n_kv_heads=8, head_dim=128, ctx=128000,
+                              dtype="f16", kv_dtype="e4m3", kv_gain=64.0, seed=1007, layers=32),
     # short query block (speculative verification of 4 draft tokens)
     "query_block_q4": dict(batch=4, n_q_heads=32, n_kv_heads=8, head_dim=128, ctx=32768,
                            q_len=4, dtype="bf16", seed=1006),
@@ -95,6 +101,21 @@ def randn_chunked(shape, dtype: str, seed: int, device="cpu", gain: float = 1.0)
         x = torch.randn(*shape[1:], generator=g, device=device, dtype=torch.float32)
         if gain != 1.0:
             x.mul_(gain)
+        out[i].copy_(x)
+        del x
+    return out
+
+
+def randn_fp8(shape, seed: int, device="cpu", gain: float = 1.0):
+    """N(0, gain^2) draws clamped to the E4M3 range (+-448) and stored as
+    torch.float8_e4m3fn, drawn one leading index at a time like randn_chunked."""
+    import torch
+    out = torch.empty(*shape, dtype=torch.float8_e4m3fn, device=device)
+    g = torch.Generator(device=device)
+    for i in range(shape[0]):
+        g.manual_seed(int(seed) * 1000003 + i)
+        x = torch.randn(*shape[1:], generator=g, device=device, dtype=torch.float32)
+        x.mul_(gain).clamp_(-448.0, 448.0)
         out[i].copy_(x)
         del x
     return out

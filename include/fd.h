@@ -47,7 +47,8 @@
  *    reading the split's K/V once.
  *  - Supported shapes: head_dim 128; G = n_q_heads / n_kv_heads and q_len
  *    with G*q_len <= 256 and q_len <= 16 (with FD_FLAG_CUDA_CORES: G in
- *    {1, 2, 4, 8} and q_len = 1); kv_dtype FD_F16 or FD_BF16;
+ *    {1, 2, 4, 8}, q_len = 1 and a 16-bit cache); kv_dtype FD_F16, FD_BF16 or
+ *    FD_E4M3;
  *    1 <= n_splits <= 128.  Other shapes return FD_ERR_UNSUPPORTED.
  */
 #ifndef FD_H_
@@ -60,7 +61,7 @@
 extern "C" {
 #endif
 
-#define FD_ABI_VERSION 2
+#define FD_ABI_VERSION 3
 #define FD_MAX_SPLITS 128   /* the split-count heuristic's cap ("Flash-Decoding ...", §6) */
 #define FD_TILE_TOKENS 128  /* split ranges are whole 128-token tiles; the planner's KV block */
 
@@ -74,7 +75,11 @@ typedef enum fd_status {
     FD_ERR_DEVICE_BOUNDS = -6     /* a seqlen or block-table entry was out of range (device status word) */
 } fd_status;
 
-typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
+/* FD_E4M3: an 8-bit floating-point cache (OCP FP8 E4M3, "fn": no infinities,
+ * largest 448).  With it, key j = k_scale * stored key and value j = v_scale *
+ * stored value (one scale per tensor, fd_desc.k_scale / v_scale), q has
+ * fd_desc.q_dtype (FD_F16 or FD_BF16), and the tensor-core path is used. */
+typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2, FD_E4M3 = 3 } fd_dtype;
 
 /* fd_desc.flags bits.  By default the split kernel computes the packed
  * group's QK^T and PV on the tensor cores (warp-level MMA, f32 accumulate).
@@ -106,13 +111,14 @@ typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2 } fd_dtype;
  *          ("Flash-Decoding ...", §7 paged-KV row).
  * v_* strides describe v_cache the same way.
  * Alignment (TMA): cache base addresses 16-byte aligned and every stride a
- * multiple of 8 elements (16 bytes); q rows 16-byte aligned. */
+ * multiple of 16 bytes (8 elements of 16 bits, 16 of FD_E4M3); q rows
+ * 16-byte aligned. */
 typedef struct fd_desc {
     int32_t batch;              /* B >= 0; B = 0 enqueues nothing */
     int32_t n_q_heads;          /* Hq >= 1 */
     int32_t n_kv_heads;         /* Hkv >= 1, divides Hq */
     int32_t head_dim;           /* D; 128 */
-    int32_t kv_dtype;           /* fd_dtype of q, K and V: FD_F16 or FD_BF16 */
+    int32_t kv_dtype;           /* fd_dtype of K and V: FD_F16, FD_BF16 (q too) or FD_E4M3 */
     int32_t out_dtype;          /* fd_dtype of out: FD_F32, FD_F16 or FD_BF16 */
     int64_t q_stride_b, q_stride_h;
     int64_t k_stride_b, k_stride_h, k_stride_t;
@@ -125,6 +131,10 @@ typedef struct fd_desc {
     int32_t flags;              /* 0, or FD_FLAG_* bits */
     int32_t q_len;              /* query positions per sequence; 0 or 1 = one (plain decode) */
     int64_t q_stride_t;         /* elements between query positions (q_len > 1) */
+    int32_t q_dtype;            /* kv_dtype FD_E4M3: fd_dtype of q (FD_F16 or FD_BF16); else unused */
+    int32_t reserved;           /* must be 0 */
+    float k_scale;              /* kv_dtype FD_E4M3: key = k_scale * stored value; else unused */
+    float v_scale;              /* kv_dtype FD_E4M3: value = v_scale * stored value; else unused */
 } fd_desc;
 
 /* ABI version of the loaded library (FD_ABI_VERSION at build time). */

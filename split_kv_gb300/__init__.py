@@ -33,7 +33,7 @@ FD_ERR_CUDA = -4
 FD_ERR_DEVICE_TIMEOUT = -5
 FD_ERR_DEVICE_BOUNDS = -6
 
-FD_F16, FD_BF16, FD_F32 = 0, 1, 2
+FD_F16, FD_BF16, FD_F32, FD_E4M3 = 0, 1, 2, 3
 FD_MAX_SPLITS = 128
 FD_TILE_TOKENS = 128
 FD_STATIC_WORKSPACE_BYTES = 8 << 20
@@ -62,6 +62,8 @@ class FdDesc(ctypes.Structure):
         ("max_seqlen", ctypes.c_int32), ("n_splits", ctypes.c_int32),
         ("flags", ctypes.c_int32), ("q_len", ctypes.c_int32),
         ("q_stride_t", ctypes.c_int64),
+        ("q_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
     def copy(self) -> "FdDesc":
@@ -214,16 +216,20 @@ def fd_device_status(stream=None, clear: bool = True) -> int:
 # ---------------------------------------------------------------- helpers
 def _dtype_code(t) -> int:
     import torch
-    return {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float32: FD_F32}[t]
+    codes = {torch.float16: FD_F16, torch.bfloat16: FD_BF16, torch.float32: FD_F32}
+    if hasattr(torch, "float8_e4m3fn"):
+        codes[torch.float8_e4m3fn] = FD_E4M3
+    return codes[t]
 
 
 def make_desc(q, k_cache, v_cache, *, n_kv_heads: int | None = None, page_size: int = 0,
               max_pages_per_seq: int = 0, max_seqlen: int = 0, n_splits: int = 0,
-              out_dtype=None) -> FdDesc:
+              out_dtype=None, k_scale: float = 1.0, v_scale: float = 1.0) -> FdDesc:
     """Descriptor for q [B, Hq, D] (or a query block [B, q_len, Hq, D]) and a
     cache given as 4-D strided tensors: contiguous [B, Hkv, T, D] (page_size 0)
     or a paged pool [P, Hkv, page, D] (any strided view of that shape, e.g. a
-    permuted [P, page, Hkv, D])."""
+    permuted [P, page, Hkv, D]).  An fp8 cache (torch.float8_e4m3fn) takes
+    k_scale / v_scale: key = k_scale * stored, value = v_scale * stored."""
     import torch
     d = FdDesc()
     if q.dim() == 4:
@@ -253,4 +259,7 @@ def make_desc(q, k_cache, v_cache, *, n_kv_heads: int | None = None, page_size: 
     d.max_seqlen = int(max_seqlen)
     d.n_splits = int(n_splits)
     d.flags = 0
+    d.q_dtype = _dtype_code(q.dtype)
+    d.reserved = 0
+    d.k_scale, d.v_scale = float(k_scale), float(v_scale)
     return d

@@ -35,7 +35,15 @@ WsLayout ws_layout(int64_t rows, int64_t splits) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool stride_ok(int64_t s) { return s >= 0 && s % 8 == 0 && s < (int64_t(1) << 38); }
+// A stride in elements of `esize` bytes is usable by TMA: a multiple of 16 bytes.
+bool stride_ok(int64_t s, int esize = 2) {
+    return s >= 0 && (s * esize) % 16 == 0 && s < (int64_t(1) << 38);
+}
+
+bool is_fp8(const fd_desc* d) { return d->kv_dtype == FD_E4M3; }
+int cache_esize(const fd_desc* d) { return is_fp8(d) ? 1 : 2; }
+// the type of q (and of the MMA operands): kv_dtype, or q_dtype for an fp8 cache
+int q_type_of(const fd_desc* d) { return is_fp8(d) ? d->q_dtype : d->kv_dtype; }
 
 int q_len_of(const fd_desc* d) { return d->q_len <= 1 ? 1 : d->q_len; }
 
@@ -57,8 +65,14 @@ fd_status check_desc(const fd_desc* d) {
     if (d->batch < 0 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1)
         return FD_ERR_INVALID_ARG;
     if (d->n_q_heads % d->n_kv_heads != 0) return FD_ERR_INVALID_ARG;
-    if (d->kv_dtype != FD_F16 && d->kv_dtype != FD_BF16)
+    if (d->kv_dtype != FD_F16 && d->kv_dtype != FD_BF16 && d->kv_dtype != FD_E4M3)
         return d->kv_dtype == FD_F32 ? FD_ERR_UNSUPPORTED : FD_ERR_INVALID_ARG;
+    if (d->reserved != 0) return FD_ERR_INVALID_ARG;
+    if (is_fp8(d)) {
+        if (d->q_dtype != FD_F16 && d->q_dtype != FD_BF16) return FD_ERR_INVALID_ARG;
+        if (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)) return FD_ERR_INVALID_ARG;
+        if ((d->flags & FD_FLAG_CUDA_CORES) != 0) return FD_ERR_UNSUPPORTED;
+    }
     if (d->out_dtype != FD_F16 && d->out_dtype != FD_BF16 && d->out_dtype != FD_F32)
         return FD_ERR_INVALID_ARG;
     if (d->head_dim != kHeadDim) return FD_ERR_UNSUPPORTED;
@@ -80,9 +94,10 @@ fd_status check_desc(const fd_desc* d) {
     }
     if (d->kv_extent < 1 || d->kv_extent > INT32_MAX) return FD_ERR_INVALID_ARG;
     if (!stride_ok(d->q_stride_b) || !stride_ok(d->q_stride_h)) return FD_ERR_INVALID_ARG;
-    if (!stride_ok(d->k_stride_b) || !stride_ok(d->k_stride_h) || !stride_ok(d->k_stride_t))
+    const int es = cache_esize(d);
+    if (!stride_ok(d->k_stride_b, es) || !stride_ok(d->k_stride_h, es) || !stride_ok(d->k_stride_t, es))
         return FD_ERR_INVALID_ARG;
-    if (!stride_ok(d->v_stride_b) || !stride_ok(d->v_stride_h) || !stride_ok(d->v_stride_t))
+    if (!stride_ok(d->v_stride_b, es) || !stride_ok(d->v_stride_h, es) || !stride_ok(d->v_stride_t, es))
         return FD_ERR_INVALID_ARG;
     if (d->k_stride_t < kHeadDim || d->v_stride_t < kHeadDim) return FD_ERR_INVALID_ARG;
     if (d->max_seqlen < 0) return FD_ERR_INVALID_ARG;
@@ -119,7 +134,8 @@ EncodeTiledFn encode_fn() {
 }
 
 // 4-D map over one cache: dims (head_dim, tokens, kv heads, sequences|pages),
-// box (64 dims, rows tokens, 1, 1), 128-byte swizzle, zero fill outside.
+// 128-byte swizzle, zero fill outside.  Box: (64 dims, rows, 1, 1) of 16-bit
+// elements, or (128 dims, rows, 1, 1) of 8-bit ones -- 128 bytes a row either way.
 fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t sb, int64_t sh,
                    int64_t st) {
     EncodeTiledFn enc = encode_fn();
@@ -133,12 +149,14 @@ fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t
                           static_cast<cuuint64_t>(d->n_kv_heads), static_cast<cuuint64_t>(n_outer)};
     // byte strides of dims 1..3; a stride of a size-1 dim is never used, but
     // must still be a valid multiple of 16
-    auto bs = [](int64_t s) { return static_cast<cuuint64_t>((s > 0 ? s : 8) * 2); };
+    const int es = cache_esize(d);
+    auto bs = [es](int64_t s) { return static_cast<cuuint64_t>(s > 0 ? s * es : 16); };
     cuuint64_t strides[3] = {bs(st), bs(sh), bs(sb)};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), 1, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(rows), 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUtensorMapDataType dt =
-        d->kv_dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = is_fp8(d) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : d->kv_dtype == FD_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -191,12 +209,16 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     // TMA box never crosses a page and paged and contiguous caches split alike
     p.split_unit = paged && d->page_size < fdk::kSplitUnit ? d->page_size : fdk::kSplitUnit;
     p.drop_first_stage = (d->flags & FD_FLAG_TEST_DROP_FIRST_STAGE) != 0 ? 1 : 0;
-    p.score_scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)));
+    // fp8 cache: key = k_scale x stored, so the scale folds into the score
+    // scale; value = v_scale x stored, applied to the split's u
+    p.score_scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kHeadDim)) *
+                                            (is_fp8(d) ? static_cast<double>(d->k_scale) : 1.0));
+    p.v_scale = is_fp8(d) ? d->v_scale : 1.0f;
     char* ws = static_cast<char*>(workspace);
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);
     p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
     p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
-    const cudaError_t e = fdk::launch_split(tmK, tmV, p, d->kv_dtype,
+    const cudaError_t e = fdk::launch_split(tmK, tmV, p, q_type_of(d), is_fp8(d),
                                             (d->flags & FD_FLAG_CUDA_CORES) != 0, d->batch,
                                             d->n_kv_heads, stream);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;

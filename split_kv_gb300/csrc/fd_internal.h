@@ -41,7 +41,8 @@ struct SplitParams {
     int32_t n_splits;
     int32_t split_unit;             // split ranges are whole units of this many tokens
     int32_t drop_first_stage;       // test hook: never request stage 0 (the wait for it times out)
-    float score_scale_log2;         // log2(e) / sqrt(D)
+    float score_scale_log2;         // log2(e) / sqrt(D), times k_scale for an fp8 cache
+    float v_scale;                  // values are v_scale x the stored ones (1 unless fp8)
     float* ws_u;                    // [rows][n_splits][D]
     float* ws_m;                    // [rows][n_splits]
     float* ws_l;                    // [rows][n_splits]
@@ -58,7 +59,7 @@ struct CombineParams {
     int32_t out_dtype;              // 0 f16, 1 bf16, 2 f32
 };
 
-size_t split_smem_bytes();
+size_t split_smem_bytes(bool fp8);
 
 // Launches `kern` with programmatic stream serialization, so that it may
 // start while the previous kernel in the stream finishes; the kernel itself
@@ -82,9 +83,10 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
 }
 
 // Launchers return cudaGetLastError() after the launch.
+// q_dtype 0 fp16 / 1 bf16; fp8: the cache holds e4m3 (tensor cores only);
 // cuda_cores selects the CUDA-core (FP32 FMA) consumer instead of the tensor-core one.
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, bool cuda_cores, int batch, int n_kv_heads,
+                         int q_dtype, bool fp8, bool cuda_cores, int batch, int n_kv_heads,
                          cudaStream_t stream);
 
 // CTAs per (split, KV head) for G * q_len columns.

@@ -30,6 +30,7 @@
 //    (bounded) and returns without writing states.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "fd_device.cuh"
 #include "fd_internal.h"
@@ -146,13 +147,31 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 
 }  // namespace
 
-size_t split_smem_bytes() { return static_cast<size_t>(kSmemUsed) + 1024; }
+// Map of the fp8-cache variant: 4 stages of [64 tokens x 128 dims] e4m3 K and
+// V boxes (16 KB), then a private 16-bit staging tile per consumer warp
+// ([K lo, K hi, V lo, V hi] x [16 rows x 128 B]) that the warp converts its
+// rows into before running the tensor-core tile on them.
+constexpr int kStagesF8 = 4;
+constexpr int kTileBytesF8 = kSub * 128;                          // one e4m3 box: 64 rows x 128 B
+constexpr int kStageBytesF8 = 2 * kTileBytesF8;                   // K, V
+constexpr int kStagingHalf = 16 * 128;                            // 16 rows x 64 dims, 16-bit
+constexpr int kStagingBytes = 4 * kStagingHalf;                   // per warp
+constexpr int kOffStagingF8 = kStagesF8 * kStageBytesF8;
+constexpr int kOffBarsF8 = kOffStagingF8 + kConsumerWarps * kStagingBytes;
+constexpr int kOffFlagF8 = kOffBarsF8 + 128;
+constexpr int kSmemUsedF8 = kOffFlagF8 + 16;
+static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffStagingF8, "merge area must fit");
+
+size_t split_smem_bytes(bool fp8) {
+    return static_cast<size_t>(fp8 ? kSmemUsedF8 : kSmemUsed) + 1024;
+}
 
 // Everything a CTA knows about its split, shared by the producer and consumers.
 struct SplitCtx {
     const SplitParams* p;
     uint8_t* smem;
     uint32_t bar0;
+    int stages;                 // ring depth (the empty barriers follow the full ones)
     volatile int* abort_flag;   // any warp gave up
     volatile int* cons_abort;   // a consumer warp gave up
     int b, kvh, split;
@@ -161,14 +180,19 @@ struct SplitCtx {
     int tok0, tok1, n_sub;
 
     __device__ __forceinline__ uint32_t full_bar(int s) const { return bar0 + 8u * s; }
-    __device__ __forceinline__ uint32_t empty_bar(int s) const { return bar0 + 8u * (kStages + s); }
+    __device__ __forceinline__ uint32_t empty_bar(int s) const { return bar0 + 8u * (stages + s); }
 };
 
 // ---------------------------------------------------------------------------
-// Producer warp: streams the split's K/V stages with TMA.
+// Producer warp: streams the split's K/V stages with TMA.  16-bit caches: four
+// [rows x 64 dims] boxes per stage (K, V low and high halves); fp8 caches
+// (F8): two [rows x 128 dims] boxes (K, V).
 // ---------------------------------------------------------------------------
+template <bool F8>
 __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tmK,
                                         const CUtensorMap* tmV, int lane) {
+    constexpr int kStages = F8 ? kStagesF8 : fdk::kStages;
+    constexpr int kStageBytes = F8 ? kStageBytesF8 : fdk::kStageBytes;
     const SplitParams& p = *c.p;
     const uint64_t policy = policy_evict_first();
     const bool paged = p.page_size != 0;
@@ -207,7 +231,15 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
         }
         if (lane == 0) mbar_arrive_expect_tx(bar, kStageBytes);
         __syncwarp();
-        if (!paged) {
+        if (F8) {
+            if (lane < (paged ? nbox : 1)) {
+                const int row = paged ? (tok + lane * rows) & (p.page_size - 1) : tok;
+                const int outer = paged ? page : c.b;
+                const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
+                tma_load_4d_hint(dst + off, tmK, bar, 0, row, c.kvh, outer, policy);
+                tma_load_4d_hint(dst + kTileBytesF8 + off, tmV, bar, 0, row, c.kvh, outer, policy);
+            }
+        } else if (!paged) {
             if (lane == 0) {
                 tma_load_4d_hint(dst + 0 * kHalfBytes, tmK, bar, 0, tok, c.kvh, c.b, policy);
                 tma_load_4d_hint(dst + 1 * kHalfBytes, tmK, bar, 64, tok, c.kvh, c.b, policy);
@@ -466,11 +498,44 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <typename T, int NB>
+// 16 e4m3 values -> 16 values of T (exact: every e4m3 value is a T value)
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    if constexpr (std::is_same<T, __half>::value) {
+        return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    } else {
+        __half2 hh;
+        memcpy(&hh, &h, 4);
+        const float2 f = __half22float2(hh);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+        uint32_t r;
+        memcpy(&r, &b, 4);
+        return r;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void e4m3x16_to(const uint4& in, uint4& lo, uint4& hi) {
+    lo = make_uint4(e4m3x2_to<T>(in.x & 0xffffu), e4m3x2_to<T>(in.x >> 16),
+                    e4m3x2_to<T>(in.y & 0xffffu), e4m3x2_to<T>(in.y >> 16));
+    hi = make_uint4(e4m3x2_to<T>(in.z & 0xffffu), e4m3x2_to<T>(in.z >> 16),
+                    e4m3x2_to<T>(in.w & 0xffffu), e4m3x2_to<T>(in.w >> 16));
+}
+
+// F8: the cache holds e4m3; each warp converts its 16 rows of a stage into its
+// staging tile (V rows past the end as zeros), releases the stage, and runs
+// the same tile code on the staging tile.
+template <typename T, int NB, bool F8>
 __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) {
+    constexpr int kStages = F8 ? kStagesF8 : fdk::kStages;
+    constexpr int kStageBytes = F8 ? kStageBytesF8 : fdk::kStageBytes;
+    constexpr int kHalf = F8 ? kStagingHalf : kHalfBytes;   // bytes between the 64-dim halves
     const SplitParams& p = *c.p;
     const int gid = lane >> 2, tig = lane & 3;
     const int r0 = cw * 16;                      // the warp's 16 rows of each stage
+    const int tr0 = F8 ? 0 : r0;                 // ... and of the tile the MMAs read
+    uint8_t* staging = c.smem + kOffStagingF8 + cw * kStagingBytes;
     const int G = p.group;
 
     // Q^T as the B operand of N block j: column 8j + gid,
@@ -516,10 +581,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 
     // ldmatrix row addresses (bytes within a half box, before the stage base)
     // K (A operand, not transposed): matrix j = lane/8 holds tokens +0/+8 and dims +0/+8
-    const int k_row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int k_row = tr0 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int k_csel = lane >> 4;
     // V^T (A operand via .trans): matrix j holds tokens +0/+8 (j/2) and dims +0/+8 (j%2)
-    const int v_row = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int v_row = tr0 + (lane & 7) + ((lane >> 4) & 1) * 8;
     const int v_csel = (lane >> 3) & 1;
 
 #pragma unroll 1
@@ -535,9 +600,39 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         const int stage_tok = c.tok0 + it * kSub;
         const int nvalid = min(kSub, c.tok1 - stage_tok);
 
+        uint32_t kbase, vbase;
+        if constexpr (F8) {
+            // convert the warp's rows: 2 tensors x 16 rows x 8 chunks of 16 e4m3
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+                const int idx = lane + 32 * k8;
+                const int tsr = idx >> 7;              // 0: K, 1: V
+                const int row = (idx >> 3) & 15;       // row of the warp's 16
+                const int c8 = idx & 7;                // dims 16*c8 .. 16*c8+15
+                const int sr = r0 + row;               // row of the stage
+                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                if (tsr == 0 || sr < nvalid) {         // V past the end stays zero
+                    const uint4 raw = *reinterpret_cast<const uint4*>(
+                        sb + tsr * kTileBytesF8 + sr * 128 + ((c8 ^ (sr & 7)) << 4));
+                    e4m3x16_to<T>(raw, lo, hi);
+                }
+                uint8_t* dst = staging + tsr * 2 * kStagingHalf + (c8 >> 2) * kStagingHalf + row * 128;
+                const int cc = (2 * c8) & 7;
+                *reinterpret_cast<uint4*>(dst + ((cc ^ (row & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(dst + (((cc + 1) ^ (row & 7)) << 4)) = hi;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(c.empty_bar(st));   // the stage is free once converted
+            kbase = smem_u32(staging);
+            vbase = smem_u32(staging + 2 * kStagingHalf);
+        } else {
+            kbase = smem_u32(sb);
+            vbase = smem_u32(sb + 2 * kHalfBytes);
+        }
+
         // Rows past the sequence end hold whatever the cache holds there; P is
         // 0 for them, but 0 * NaN would still poison PV, so zero those V rows.
-        if (nvalid < r0 + 16) {
+        if (!F8 && nvalid < r0 + 16) {
             uint8_t* vb = sb + 2 * kHalfBytes;
 #pragma unroll
             for (int idx = lane; idx < 16 * 16; idx += 32) {
@@ -555,11 +650,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         float s[NB][4];
 #pragma unroll
         for (int j = 0; j < NB; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-        const uint32_t kbase = smem_u32(sb);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             const int chunk = 2 * kb + k_csel;                     // 16-byte chunk of the row
-            const uint32_t addr = kbase + (chunk >> 3) * kHalfBytes + k_row * 128 +
+            const uint32_t addr = kbase + (chunk >> 3) * kHalf + k_row * 128 +
                                   (((chunk & 7) ^ (k_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4(a, addr);
@@ -621,11 +715,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         }
 
         // ---- O^T += V^T . P^T
-        const uint32_t vbase = smem_u32(sb + 2 * kHalfBytes);
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
             const int chunk = 2 * mb + v_csel;
-            const uint32_t addr = vbase + (chunk >> 3) * kHalfBytes + v_row * 128 +
+            const uint32_t addr = vbase + (chunk >> 3) * kHalf + v_row * 128 +
                                   (((chunk & 7) ^ (v_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4_trans(a, addr);
@@ -636,7 +729,7 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(c.empty_bar(st));
+        if (!F8 && lane == 0) mbar_arrive(c.empty_bar(st));
     }
 
     // lane sums -> column sums over the 8 token rows (lanes with equal tig)
@@ -671,18 +764,25 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 }
 
 // ---------------------------------------------------------------------------
-// The split kernel.  CONSUME is consume_tc<T, NB> (default) or
+// The split kernel.  The consumer is consume_tc<T, NB, F8> (default) or
 // consume_simt<T, G>; both leave per-warp states of up to 16 columns for the
 // final merge.
 // ---------------------------------------------------------------------------
 template <typename T, int KIND>
 struct Consumer;
-// KIND 1, 2: tensor cores with 8 or 16 columns; KIND 10 + G: CUDA cores, group G
+// KIND 1, 2: tensor cores with 8 or 16 columns; 21, 22: the same on an fp8
+// cache; KIND 10 + G: CUDA cores, group G
 template <typename T> struct Consumer<T, 1> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1, false>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 2> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2, false>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 21> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1, true>(c, w, l); }
+};
+template <typename T> struct Consumer<T, 22> {
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2, true>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 11> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 1>(c, w, l); }
@@ -701,11 +801,14 @@ template <typename T, int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    constexpr bool F8 = KIND >= 20;
+    constexpr int kRing = F8 ? kStagesF8 : kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     SplitCtx c;
+    c.stages = kRing;
     c.p = &p;
     c.smem = smem;
     c.split = blockIdx.x;
@@ -716,12 +819,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
 
-    c.bar0 = smem_u32(smem + kOffBars);
-    c.abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
-    c.cons_abort = reinterpret_cast<volatile int*>(smem + kOffFlag + 4);
+    c.bar0 = smem_u32(smem + (F8 ? kOffBarsF8 : kOffBars));
+    c.abort_flag = reinterpret_cast<volatile int*>(smem + (F8 ? kOffFlagF8 : kOffFlag));
+    c.cons_abort = reinterpret_cast<volatile int*>(smem + (F8 ? kOffFlagF8 : kOffFlag) + 4);
     if (threadIdx.x == 0) {
 #pragma unroll
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRing; ++s) {
             mbar_init(c.full_bar(s), 1);
             mbar_init(c.empty_bar(s), kConsumerWarps);
         }
@@ -759,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
 
     if (warp == kConsumerWarps) {
-        produce(c, &tmK, &tmV, lane);
+        produce<F8>(c, &tmK, &tmV, lane);
         return;
     }
 
@@ -792,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int64_t row = (static_cast<int64_t>(c.b) * p.q_len + i) * p.n_q_heads +
                             c.kvh * p.group + g;
         const int64_t idx = row * S + c.split;
-        p.ws_u[idx * kHeadDim + d] = u;
+        p.ws_u[idx * kHeadDim + d] = u * p.v_scale;   // values are v_scale x the stored ones
         if (d == 0) {
             p.ws_m[idx] = m_out;
             p.ws_l[idx] = l;
@@ -805,7 +908,7 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
     auto kern = fd_split_kernel<T, KIND>;
-    const size_t smem = split_smem_bytes();
+    const size_t smem = split_smem_bytes(KIND >= 20);
     // one attribute call per (kernel, device): cheap and safe to repeat
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -822,8 +925,11 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
 
 template <typename T>
 static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                   const SplitParams& p, bool cuda_cores, int batch,
+                                   const SplitParams& p, bool fp8, bool cuda_cores, int batch,
                                    int n_kv_heads, cudaStream_t stream) {
+    if (fp8)
+        return p.cols <= 8 ? launch_split_t<T, 21>(tmK, tmV, p, batch, n_kv_heads, stream)
+                           : launch_split_t<T, 22>(tmK, tmV, p, batch, n_kv_heads, stream);
     if (cuda_cores) {
         switch (p.group) {
             case 1: return launch_split_t<T, 11>(tmK, tmV, p, batch, n_kv_heads, stream);
@@ -838,11 +944,11 @@ static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tm
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
-                         int kv_dtype, bool cuda_cores, int batch, int n_kv_heads,
+                         int q_dtype, bool fp8, bool cuda_cores, int batch, int n_kv_heads,
                          cudaStream_t stream) {
-    if (kv_dtype == 0)
-        return launch_split_dt<__half>(tmK, tmV, p, cuda_cores, batch, n_kv_heads, stream);
-    return launch_split_dt<__nv_bfloat16>(tmK, tmV, p, cuda_cores, batch, n_kv_heads, stream);
+    if (q_dtype == 0)
+        return launch_split_dt<__half>(tmK, tmV, p, fp8, cuda_cores, batch, n_kv_heads, stream);
+    return launch_split_dt<__nv_bfloat16>(tmK, tmV, p, fp8, cuda_cores, batch, n_kv_heads, stream);
 }
 
 cudaError_t read_status(unsigned* value, cudaStream_t stream, bool clear) {

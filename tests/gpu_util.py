@@ -45,7 +45,8 @@ class Guarded:
 
 
 def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=None,
-               n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True, flags=0):
+               n_splits=0, out_dtype=torch.float32, stream=None, check_guards=True, flags=0,
+               k_scale=1.0, v_scale=1.0):
     """fd_decode through the C ABI; returns (out [rows, D] f64, lse [rows] f64, S)
     with rows = B*q_len*Hq (q is [B, Hq, D] or a query block [B, q_len, Hq, D])."""
     dev = q.device
@@ -62,7 +63,7 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
         mp = block_table.shape[1]
     desc = fd.make_desc(q, k, v, n_kv_heads=n_kv_heads, page_size=page_size, max_pages_per_seq=mp,
                         max_seqlen=int(seqlens_h.max()) if B else 0, n_splits=n_splits,
-                        out_dtype=out_dtype)
+                        out_dtype=out_dtype, k_scale=k_scale, v_scale=v_scale)
     desc.flags = flags
     if n_splits > 0:
         S = n_splits
@@ -111,9 +112,11 @@ def assert_parity(got_o, got_l, ref_o, ref_l, what=""):
     return float(err.max()) if err.size else 0.0
 
 
-def oracle_all(q, k, v, seqlens_h, dtype, n_kv_heads, page_size=0, block_table=None, rows=None):
+def oracle_all(q, k, v, seqlens_h, dtype, n_kv_heads, page_size=0, block_table=None, rows=None,
+               kv_dtype=None, k_scale=1.0, v_scale=1.0):
     return oracle.decode(q.cpu(), k.cpu(), v.cpu(), seqlens_h, dtype=dtype, n_kv_heads=n_kv_heads,
-                         page_size=page_size, block_table=block_table, rows=rows)
+                         page_size=page_size, block_table=block_table, rows=rows,
+                         kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 def oracle_rows_contiguous(q, k, v, seqlens_h, rows, dtype):

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(fd):
 
 
 def test_abi_version_and_strings(fd):
-    assert fd.fd_abi_version() == 2
+    assert fd.fd_abi_version() == 3
     for code in range(-6, 1):
         s = fd.fd_status_string(code)
         assert s and s != "unknown status"
@@ -45,9 +45,10 @@ def test_abi_version_and_strings(fd):
 
 
 def test_desc_struct_size_matches_header(fd):
-    # 6 int32 + 9 int64 + 6 int32 + 1 int64 = 24 + 72 + 24 + 8 = 128 bytes
-    assert ctypes.sizeof(fd.FdDesc) == 128
+    # 6 int32 + 9 int64 + 6 int32 + 1 int64 + 2 int32 + 2 float = 144 bytes
+    assert ctypes.sizeof(fd.FdDesc) == 144
     assert fd.FdDesc.q_stride_t.offset == 120
+    assert fd.FdDesc.k_scale.offset == 136 and fd.FdDesc.v_scale.offset == 140
 
 
 def test_plan_splits_matches_oracle_table(fd, golden_dir):
@@ -145,6 +146,12 @@ def test_decode_rejects_bad_arguments_without_a_gpu(fd):
     assert call(_desc(fd, n_q_heads=8 * 40, q_len=8, q_stride_t=320 * 128)) == fd.FD_ERR_UNSUPPORTED
     assert call(_desc(fd, q_len=-1)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, q_len=4, q_stride_t=100)) == fd.FD_ERR_INVALID_ARG
+    e4 = dict(kv_dtype=fd.FD_E4M3, q_dtype=fd.FD_F16, k_scale=0.5, v_scale=2.0)
+    assert call(_desc(fd, **dict(e4, q_dtype=fd.FD_E4M3))) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, **dict(e4, k_scale=float("inf")))) == fd.FD_ERR_INVALID_ARG
+    assert call(_desc(fd, **e4, flags=cc)) == fd.FD_ERR_UNSUPPORTED          # fp8 on CUDA cores
+    assert call(_desc(fd, **e4, k_stride_t=136)) == fd.FD_ERR_INVALID_ARG    # 136 B: not a 16 B multiple
+    assert call(_desc(fd, reserved=1)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, n_q_heads=20)) == fd.FD_ERR_INVALID_ARG           # 8 does not divide 20
     assert call(_desc(fd, kv_dtype=fd.FD_F32)) == fd.FD_ERR_UNSUPPORTED
     assert call(_desc(fd, kv_dtype=7)) == fd.FD_ERR_INVALID_ARG

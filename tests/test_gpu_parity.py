@@ -496,3 +496,73 @@ def test_other_group_sizes_single_query(group):
     for S in (0, 7):
         got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
         assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} S={S}")
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) caches
+FP8 = hasattr(torch, "float8_e4m3fn")
+fp8_only = pytest.mark.skipif(not FP8, reason="torch without float8_e4m3fn")
+GAIN_K, GAIN_V = 64.0, 16.0          # stored = value x gain, scale = 1 / gain
+
+
+def _nan_past_lengths_fp8(t, lens):
+    """E4M3 NaN (0x7f) in every cache slot past each sequence's length."""
+    raw = t.view(torch.uint8)
+    for b, L in enumerate(lens):
+        raw[b, :, L:] = 0x7F
+
+
+@fp8_only
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_fp8_cache(q_dtype, group):
+    B, Hkv, D, T = 3, 2, 128, 2100
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, Hq, D), q_dtype, 1800 + group, device=DEV)
+    k8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1810 + group, device=DEV, gain=GAIN_K)
+    v8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1820 + group, device=DEV, gain=GAIN_V)
+    lens = [2100, 130, 1]
+    _nan_past_lengths_fp8(k8, lens)
+    _nan_past_lengths_fp8(v8, lens)
+    sl = np.array(lens, dtype=np.int32)
+    sc = dict(k_scale=1 / GAIN_K, v_scale=1 / GAIN_V)
+    ref_o, ref_l = oracle_all(q, k8, v8, sl, q_dtype, Hkv, kv_dtype="e4m3", **sc)
+    for S in (0, 3, 128):
+        got_o, got_l, _ = run_decode(q, k8, v8, sl, n_splits=S, **sc)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 q={q_dtype} G={group} S={S}")
+
+
+@fp8_only
+@pytest.mark.parametrize("ps", [16, 64])
+def test_fp8_paged_and_query_block(ps):
+    """An fp8 pool read through a shuffled block table, with a 4-position
+    query block of a G = 4 group (16 columns: two MMA N blocks)."""
+    B, Hkv, G, D, ql = 2, 2, 4, 128, 4
+    lens = [1500, 300]
+    max_pages = -(-max(lens) // ps)
+    n_pages = B * max_pages + 3
+    pk = fd_inputs.randn_fp8((n_pages, Hkv, ps, D), 1900 + ps, device=DEV, gain=GAIN_K)
+    pv = fd_inputs.randn_fp8((n_pages, Hkv, ps, D), 1901 + ps, device=DEV, gain=GAIN_V)
+    bt = fd_inputs.page_permutation(1902 + ps, n_pages)[:B * max_pages].reshape(B, max_pages).copy()
+    q = fd_inputs.randn((B, ql, Hkv * G, D), "f16", 1903, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    sc = dict(k_scale=1 / GAIN_K, v_scale=1 / GAIN_V)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "f16", Hkv, page_size=ps, block_table=bt,
+                              kv_dtype="e4m3", **sc)
+    for S in (0, 5):
+        got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=S, **sc)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 paged ps={ps} S={S}")
+
+
+@fp8_only
+def test_fp8_long_gqa_128k_one_layer():
+    c = fd_inputs.WORKLOADS["long_gqa_128k_fp8"]
+    B, Hq, Hkv, D, T = c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"]
+    g = c["kv_gain"]
+    q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"], device=DEV)
+    k8 = fd_inputs.randn_fp8((B, Hkv, T, D), c["seed"] + 10, device=DEV, gain=g)
+    v8 = fd_inputs.randn_fp8((B, Hkv, T, D), c["seed"] + 11, device=DEV, gain=g)
+    sl = np.array([T], dtype=np.int32)
+    got_o, got_l, S = run_decode(q, k8, v8, sl, k_scale=1 / g, v_scale=1 / g)
+    ref_o, ref_l = oracle_all(q, k8, v8, sl, c["dtype"], Hkv, kv_dtype="e4m3",
+                              k_scale=1 / g, v_scale=1 / g)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 long_gqa_128k S={S}")
