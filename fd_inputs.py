@@ -52,7 +52,7 @@ WORKLOADS = {
 
 def torch_dtype(name: str):
     import torch
-    return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
 
 
 def randn(shape, dtype: str, seed: int, device="cpu", gain: float = 1.0):

@@ -147,20 +147,17 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 
 }  // namespace
 
-// Map of the fp8-cache variant: 4 stages of [64 tokens x 128 dims] e4m3 K and
-// V boxes (16 KB), then a private 16-bit staging tile per consumer warp
-// ([K lo, K hi, V lo, V hi] x [16 rows x 128 B]) that the warp converts its
-// rows into before running the tensor-core tile on them.
-constexpr int kStagesF8 = 4;
+// Map of the fp8-cache variant: 6 stages of [64 tokens x 128 dims] e4m3 K and
+// V boxes (16 KB each stage, the same bytes in flight as the 16-bit ring),
+// then the barriers.  Consumers read a stage straight into registers.
+constexpr int kStagesF8 = 6;
 constexpr int kTileBytesF8 = kSub * 128;                          // one e4m3 box: 64 rows x 128 B
 constexpr int kStageBytesF8 = 2 * kTileBytesF8;                   // K, V
-constexpr int kStagingHalf = 16 * 128;                            // 16 rows x 64 dims, 16-bit
-constexpr int kStagingBytes = 4 * kStagingHalf;                   // per warp
-constexpr int kOffStagingF8 = kStagesF8 * kStageBytesF8;
-constexpr int kOffBarsF8 = kOffStagingF8 + kConsumerWarps * kStagingBytes;
+constexpr int kOffBarsF8 = kStagesF8 * kStageBytesF8;             // full[6], empty[6]
 constexpr int kOffFlagF8 = kOffBarsF8 + 128;
 constexpr int kSmemUsedF8 = kOffFlagF8 + 16;
-static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffStagingF8, "merge area must fit");
+static_assert(2 * kStagesF8 * 8 <= 128, "barriers must fit");
+static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBarsF8, "merge area must fit");
 
 size_t split_smem_bytes(bool fp8) {
     return static_cast<size_t>(fp8 ? kSmemUsedF8 : kSmemUsed) + 1024;
@@ -498,57 +495,106 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 16 e4m3 values -> 16 values of T (exact: every e4m3 value is a T value)
-template <typename T>
-__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-    if constexpr (std::is_same<T, __half>::value) {
-        return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-    } else {
-        __half2 hh;
-        memcpy(&hh, &h, 4);
-        const float2 f = __half22float2(hh);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-        uint32_t r;
-        memcpy(&r, &b, 4);
-        return r;
+// Online softmax (base 2) of one 16-token tile for up to 8 * NB columns, and
+// P^T as hi + lo B fragments of the PV MMAs.  s holds S^T (C fragments);
+// csc[j][e] is the base-2 score scale of the lane's column 8j + 2tig + e;
+// a column sees the keys before vis[j][e] and the stage's first nvalid rows.
+// Returns whether any running max moved (the accumulators then take al).
+template <typename MT, int NB>
+__device__ __forceinline__ bool softmax_tile(const float (&s)[NB][4], const float (&csc)[NB][2],
+                                             const int (&vis)[NB][2], int nvalid, int stage_tok,
+                                             int row0, int row1, float (&m)[NB][2],
+                                             float (&l)[NB][2], float (&al)[NB][2],
+                                             uint32_t (&bh)[NB][2], uint32_t (&bl)[NB][2]) {
+    bool rescale = false;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int lim = min(nvalid, vis[j][e] - stage_tok);
+            t[e] = row0 < lim ? s[j][e] * csc[j][e] : -INFINITY;         // token gid
+            t[e + 2] = row1 < lim ? s[j][e + 2] * csc[j][e] : -INFINITY; // token gid + 8
+        }
+        float pr[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float mx = fmaxf(t[e], t[e + 2]);
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+            const float mn = fmaxf(m[j][e], mx);
+            const float mu = mn == -INFINITY ? 0.f : mn;   // never -inf - -inf
+            al[j][e] = fast_exp2(m[j][e] - mu);
+            pr[e] = fast_exp2(t[e] - mu);
+            pr[e + 2] = fast_exp2(t[e + 2] - mu);
+            l[j][e] = fmaf(al[j][e], l[j][e], pr[e] + pr[e + 2]);
+            m[j][e] = mn;
+            rescale |= al[j][e] != 1.f;
+        }
+        // P^T as B fragments: hi + lo parts, transposed in registers
+        float k0, k1, k2, k3, d0, d1, d2, d3;
+        const uint32_t hi01 = Mma<MT>::pack(pr[0], pr[1], k0, k1);
+        const uint32_t hi23 = Mma<MT>::pack(pr[2], pr[3], k2, k3);
+        const uint32_t lo01 = Mma<MT>::pack(pr[0] - k0, pr[1] - k1, d0, d1);
+        const uint32_t lo23 = Mma<MT>::pack(pr[2] - k2, pr[3] - k3, d2, d3);
+        bh[j][0] = movmatrix_trans(hi01);
+        bh[j][1] = movmatrix_trans(hi23);
+        bl[j][0] = movmatrix_trans(lo01);
+        bl[j][1] = movmatrix_trans(lo23);
     }
+    return __any_sync(kFull, rescale);
 }
 
+template <int NB>
+__device__ __forceinline__ void rescale_acc(float (&acc)[8][NB][4], const float (&al)[NB][2]) {
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            acc[mb][j][0] *= al[j][0];
+            acc[mb][j][1] *= al[j][1];
+            acc[mb][j][2] *= al[j][0];
+            acc[mb][j][3] *= al[j][1];
+        }
+}
+
+// Keys visible to the lane's C columns: column n is query position n / G and
+// sees the first L - q_len + 1 + n / G keys.
+template <int NB>
+__device__ __forceinline__ void visible_keys(const SplitCtx& c, int tig, int (&vis)[NB][2]) {
+    const SplitParams& p = *c.p;
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = c.cb * kCols + 8 * j + 2 * tig + e;
+            vis[j][e] = n < p.cols ? c.L - p.q_len + 1 + n / p.group : c.L;
+        }
+}
+
+// Start of the row of q for column n of the CTA's block (row 0 for padding columns).
 template <typename T>
-__device__ __forceinline__ void e4m3x16_to(const uint4& in, uint4& lo, uint4& hi) {
-    lo = make_uint4(e4m3x2_to<T>(in.x & 0xffffu), e4m3x2_to<T>(in.x >> 16),
-                    e4m3x2_to<T>(in.y & 0xffffu), e4m3x2_to<T>(in.y >> 16));
-    hi = make_uint4(e4m3x2_to<T>(in.z & 0xffffu), e4m3x2_to<T>(in.z >> 16),
-                    e4m3x2_to<T>(in.w & 0xffffu), e4m3x2_to<T>(in.w >> 16));
+__device__ __forceinline__ const T* q_row(const SplitCtx& c, int n, bool& real) {
+    const SplitParams& p = *c.p;
+    real = n < p.cols;
+    const int i = real ? n / p.group : 0, g = real ? n % p.group : 0;
+    return static_cast<const T*>(p.q) + static_cast<int64_t>(c.b) * p.q_sb +
+           static_cast<int64_t>(i) * p.q_st + static_cast<int64_t>(c.kvh * p.group + g) * p.q_sh;
 }
 
-// F8: the cache holds e4m3; each warp converts its 16 rows of a stage into its
-// staging tile (V rows past the end as zeros), releases the stage, and runs
-// the same tile code on the staging tile.
-template <typename T, int NB, bool F8>
+template <typename T, int NB>
 __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) {
-    constexpr int kStages = F8 ? kStagesF8 : fdk::kStages;
-    constexpr int kStageBytes = F8 ? kStageBytesF8 : fdk::kStageBytes;
-    constexpr int kHalf = F8 ? kStagingHalf : kHalfBytes;   // bytes between the 64-dim halves
     const SplitParams& p = *c.p;
     const int gid = lane >> 2, tig = lane & 3;
     const int r0 = cw * 16;                      // the warp's 16 rows of each stage
-    const int tr0 = F8 ? 0 : r0;                 // ... and of the tile the MMAs read
-    uint8_t* staging = c.smem + kOffStagingF8 + cw * kStagingBytes;
-    const int G = p.group;
 
     // Q^T as the B operand of N block j: column 8j + gid,
     // b0 = q[.][16kb + 2tig .. +1], b1 = q[.][16kb + 8 + 2tig .. +1]
     uint32_t qb[NB][8][2];
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-        const int n = c.cb * kCols + 8 * j + gid;
-        const bool real = n < p.cols;
-        const int i = real ? n / G : 0, g = real ? n % G : 0;
-        const T* qrow = static_cast<const T*>(p.q) + static_cast<int64_t>(c.b) * p.q_sb +
-                        static_cast<int64_t>(i) * p.q_st +
-                        static_cast<int64_t>(c.kvh * G + g) * p.q_sh;
+        bool real;
+        const T* qrow = q_row<T>(c, c.cb * kCols + 8 * j + gid, real);
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             const uint32_t lo = __ldg(reinterpret_cast<const unsigned int*>(qrow + 16 * kb + 2 * tig));
@@ -557,15 +603,11 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             qb[j][kb][1] = real ? hi : 0u;
         }
     }
-    // keys visible to this lane's columns: the first L - q_len + 1 + i
     int vis[NB][2];
+    visible_keys<NB>(c, tig, vis);
+    float csc[NB][2];
 #pragma unroll
-    for (int j = 0; j < NB; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = c.cb * kCols + 8 * j + 2 * tig + e;
-            vis[j][e] = n < p.cols ? c.L - p.q_len + 1 + n / G : c.L;
-        }
+    for (int j = 0; j < NB; ++j) csc[j][0] = csc[j][1] = p.score_scale_log2;
 
     float m[NB][2], l[NB][2];               // base-2 running max; this lane's share of the sums
     float acc[8][NB][4];
@@ -581,10 +623,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 
     // ldmatrix row addresses (bytes within a half box, before the stage base)
     // K (A operand, not transposed): matrix j = lane/8 holds tokens +0/+8 and dims +0/+8
-    const int k_row = tr0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int k_row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int k_csel = lane >> 4;
     // V^T (A operand via .trans): matrix j holds tokens +0/+8 (j/2) and dims +0/+8 (j%2)
-    const int v_row = tr0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+    const int v_row = r0 + (lane & 7) + ((lane >> 4) & 1) * 8;
     const int v_csel = (lane >> 3) & 1;
 
 #pragma unroll 1
@@ -599,40 +641,12 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         uint8_t* sb = c.smem + st * kStageBytes;
         const int stage_tok = c.tok0 + it * kSub;
         const int nvalid = min(kSub, c.tok1 - stage_tok);
-
-        uint32_t kbase, vbase;
-        if constexpr (F8) {
-            // convert the warp's rows: 2 tensors x 16 rows x 8 chunks of 16 e4m3
-#pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-                const int idx = lane + 32 * k8;
-                const int tsr = idx >> 7;              // 0: K, 1: V
-                const int row = (idx >> 3) & 15;       // row of the warp's 16
-                const int c8 = idx & 7;                // dims 16*c8 .. 16*c8+15
-                const int sr = r0 + row;               // row of the stage
-                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                if (tsr == 0 || sr < nvalid) {         // V past the end stays zero
-                    const uint4 raw = *reinterpret_cast<const uint4*>(
-                        sb + tsr * kTileBytesF8 + sr * 128 + ((c8 ^ (sr & 7)) << 4));
-                    e4m3x16_to<T>(raw, lo, hi);
-                }
-                uint8_t* dst = staging + tsr * 2 * kStagingHalf + (c8 >> 2) * kStagingHalf + row * 128;
-                const int cc = (2 * c8) & 7;
-                *reinterpret_cast<uint4*>(dst + ((cc ^ (row & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4*>(dst + (((cc + 1) ^ (row & 7)) << 4)) = hi;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(c.empty_bar(st));   // the stage is free once converted
-            kbase = smem_u32(staging);
-            vbase = smem_u32(staging + 2 * kStagingHalf);
-        } else {
-            kbase = smem_u32(sb);
-            vbase = smem_u32(sb + 2 * kHalfBytes);
-        }
+        const uint32_t kbase = smem_u32(sb);
+        const uint32_t vbase = smem_u32(sb + 2 * kHalfBytes);
 
         // Rows past the sequence end hold whatever the cache holds there; P is
         // 0 for them, but 0 * NaN would still poison PV, so zero those V rows.
-        if (!F8 && nvalid < r0 + 16) {
+        if (nvalid < r0 + 16) {
             uint8_t* vb = sb + 2 * kHalfBytes;
 #pragma unroll
             for (int idx = lane; idx < 16 * 16; idx += 32) {
@@ -653,7 +667,7 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             const int chunk = 2 * kb + k_csel;                     // 16-byte chunk of the row
-            const uint32_t addr = kbase + (chunk >> 3) * kHalf + k_row * 128 +
+            const uint32_t addr = kbase + (chunk >> 3) * kHalfBytes + k_row * 128 +
                                   (((chunk & 7) ^ (k_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4(a, addr);
@@ -661,64 +675,18 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             for (int j = 0; j < NB; ++j) Mma<T>::run(s[j], a, qb[j][kb][0], qb[j][kb][1]);
         }
 
-        // ---- online softmax (base 2) per column over the 16 tokens
-        const float sc = p.score_scale_log2;
-        const int row0 = r0 + gid, row1 = r0 + gid + 8;    // rows in the stage
-        bool rescale = false;
-        uint32_t bh[NB][2], bl[NB][2];
+        // ---- online softmax per column over the 16 tokens
         float al[NB][2];
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-            float t[4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int lim = min(nvalid, vis[j][e] - stage_tok);
-                t[e] = row0 < lim ? s[j][e] * sc : -INFINITY;         // token gid
-                t[e + 2] = row1 < lim ? s[j][e + 2] * sc : -INFINITY; // token gid + 8
-            }
-            float pr[4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float mx = fmaxf(t[e], t[e + 2]);
-#pragma unroll
-                for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-                const float mn = fmaxf(m[j][e], mx);
-                const float mu = mn == -INFINITY ? 0.f : mn;   // never -inf - -inf
-                al[j][e] = fast_exp2(m[j][e] - mu);
-                pr[e] = fast_exp2(t[e] - mu);
-                pr[e + 2] = fast_exp2(t[e + 2] - mu);
-                l[j][e] = fmaf(al[j][e], l[j][e], pr[e] + pr[e + 2]);
-                m[j][e] = mn;
-                rescale |= al[j][e] != 1.f;
-            }
-            // P^T as B fragments: hi + lo parts, transposed in registers
-            float k0, k1, k2, k3, d0, d1, d2, d3;
-            const uint32_t hi01 = Mma<T>::pack(pr[0], pr[1], k0, k1);
-            const uint32_t hi23 = Mma<T>::pack(pr[2], pr[3], k2, k3);
-            const uint32_t lo01 = Mma<T>::pack(pr[0] - k0, pr[1] - k1, d0, d1);
-            const uint32_t lo23 = Mma<T>::pack(pr[2] - k2, pr[3] - k3, d2, d3);
-            bh[j][0] = movmatrix_trans(hi01);
-            bh[j][1] = movmatrix_trans(hi23);
-            bl[j][0] = movmatrix_trans(lo01);
-            bl[j][1] = movmatrix_trans(lo23);
-        }
-        if (__any_sync(kFull, rescale)) {
-#pragma unroll
-            for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-                for (int j = 0; j < NB; ++j) {
-                    acc[mb][j][0] *= al[j][0];
-                    acc[mb][j][1] *= al[j][1];
-                    acc[mb][j][2] *= al[j][0];
-                    acc[mb][j][3] *= al[j][1];
-                }
-        }
+        uint32_t bh[NB][2], bl[NB][2];
+        if (softmax_tile<T, NB>(s, csc, vis, nvalid, stage_tok, r0 + gid, r0 + gid + 8, m, l, al,
+                                bh, bl))
+            rescale_acc<NB>(acc, al);
 
         // ---- O^T += V^T . P^T
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
             const int chunk = 2 * mb + v_csel;
-            const uint32_t addr = vbase + (chunk >> 3) * kHalf + v_row * 128 +
+            const uint32_t addr = vbase + (chunk >> 3) * kHalfBytes + v_row * 128 +
                                   (((chunk & 7) ^ (v_row & 7)) << 4);
             uint32_t a[4];
             ldsm_x4_trans(a, addr);
@@ -729,7 +697,7 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             }
         }
         __syncwarp();
-        if (!F8 && lane == 0) mbar_arrive(c.empty_bar(st));
+        if (lane == 0) mbar_arrive(c.empty_bar(st));
     }
 
     // lane sums -> column sums over the 8 token rows (lanes with equal tig)
@@ -764,7 +732,214 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 }
 
 // ---------------------------------------------------------------------------
-// The split kernel.  The consumer is consume_tc<T, NB, F8> (default) or
+// Consumer for an fp8 (E4M3) cache: the same swap-AB tile as f16 MMAs, with
+// the A fragments built in registers from the e4m3 stage (no ldmatrix, no
+// staging copy).  Each MMA's contraction index is permuted so that every lane
+// reads whole 16-byte chunks of the swizzled stage:
+//  - QK: lane (gid, tig) reads K bytes 32tig .. 32tig+31 of tokens gid and
+//    gid + 8.  Block kb takes dims 32tig + 4kb + {0,1} as its k = 2tig + {0,1}
+//    and dims 32tig + 4kb + {2,3} as k = 2tig + 8 + {0,1}; Q^T's fragments
+//    follow the same order, so each score is still the full dot product.
+//  - PV: lane (gid, tig) reads V bytes 16gid .. 16gid+15 of tokens 2tig,
+//    2tig+1, 2tig+8 and 2tig+9; output row gid (gid + 8) of block mb is dim
+//    16gid + 2mb (+1).  Token order is the plain one, as P^T expects.
+// e4m3 -> f16 is exact (one cvt per pair).  A bf16 Q enters as f16 after a
+// per-column power of two that puts the column's largest |q| in [2^14, 2^15)
+// (every element within 2^31 of it converts exactly); that column's score
+// scale takes the inverse power.  P goes to f16 as hi + lo parts.
+// The warp's 8 chunk loads are its only reads of a stage, so it hands the
+// stage back to the producer right after them.
+// ---------------------------------------------------------------------------
+// four e4m3 bytes -> two f16 pairs: (b0, b1) and (b2, b3), low byte in the low half
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, x;\n\tcvt.rn.f16x2.e4m3x2 %1, y;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+__device__ __forceinline__ void unpack4(const uint4& r, uint32_t* w) {
+    w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
+}
+
+template <typename T, int NB>
+__device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) {
+    const SplitParams& p = *c.p;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int r0 = cw * 16;                      // the warp's 16 rows of each stage
+
+    // Q^T of N block j (column 8j + gid) in the permuted order: b0 of block kb
+    // is q[32tig + 4kb .. +1], b1 is q[32tig + 4kb + 2 .. +3]
+    uint32_t qb[NB][8][2];
+    int qexp[NB];                                // the column's power of two
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        bool real;
+        const T* qrow = q_row<T>(c, c.cb * kCols + 8 * j + gid, real);
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const uint4 r = real ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * tig) + x)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            unpack4(r, w + 4 * x);
+        }
+        int k = 0;
+        if constexpr (!std::is_same<T, __half>::value) {
+            float mx = 0.f;
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const float2 f = Cvt<T>::pair(w[x]);
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));   // the column's 4 lanes
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+            const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+            k = (mx > 0.f && mx <= 3.402823466e38f) ? min(14 - ex, 126) : 0;
+            const float qm = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const float2 f = Cvt<T>::pair(w[x]);
+                const __half2 h = __floats2half2_rn(f.x * qm, f.y * qm);
+                memcpy(&w[x], &h, 4);
+            }
+        }
+        qexp[j] = k;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            qb[j][kb][0] = w[2 * kb];
+            qb[j][kb][1] = w[2 * kb + 1];
+        }
+    }
+    // score scale of the lane's C columns 8j + 2tig + e (held by lanes gid = 2tig + e)
+    float csc[NB][2];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int k = __shfl_sync(kFull, qexp[j], (2 * tig + e) * 4);
+            csc[j][e] = p.score_scale_log2 * __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+        }
+    int vis[NB][2];
+    visible_keys<NB>(c, tig, vis);
+
+    float m[NB][2], l[NB][2];
+    float acc[8][NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        m[j][0] = m[j][1] = -INFINITY;
+        l[j][0] = l[j][1] = 0.f;
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mb][j][e] = 0.f;
+    }
+
+    // byte offsets of the lane's chunks in a stage (128-byte rows, 128B swizzle:
+    // chunk ch of row r sits at chunk ch ^ (r & 7)); rows r and r + 8 share the phase
+    const int krow = r0 + gid;
+    const int k_off0 = krow * 128 + (((2 * tig) ^ (krow & 7)) << 4);
+    const int k_off1 = krow * 128 + (((2 * tig + 1) ^ (krow & 7)) << 4);
+    int v_row[4], v_off[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        v_row[x] = r0 + 2 * tig + (x & 1) + (x >> 1) * 8;
+        v_off[x] = kTileBytesF8 + v_row[x] * 128 + ((gid ^ (v_row[x] & 7)) << 4);
+    }
+
+#pragma unroll 1
+    for (int it = 0; it < c.n_sub; ++it) {
+        const int st = it % kStagesF8;
+        const bool ok = wait_or_flag(c.full_bar(st), (it / kStagesF8) & 1);
+        if (!__all_sync(kFull, ok)) {
+            *c.cons_abort = 1;
+            *c.abort_flag = 1;
+            break;
+        }
+        const uint8_t* sb = c.smem + st * kStageBytesF8;
+        const int stage_tok = c.tok0 + it * kSub;
+        const int nvalid = min(kSub, c.tok1 - stage_tok);
+
+        uint32_t kw[16], vw[4][4];
+        unpack4(*reinterpret_cast<const uint4*>(sb + k_off0), kw);
+        unpack4(*reinterpret_cast<const uint4*>(sb + k_off1), kw + 4);
+        unpack4(*reinterpret_cast<const uint4*>(sb + k_off0 + 8 * 128), kw + 8);
+        unpack4(*reinterpret_cast<const uint4*>(sb + k_off1 + 8 * 128), kw + 12);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) unpack4(*reinterpret_cast<const uint4*>(sb + v_off[x]), vw[x]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.empty_bar(st));   // the stage is in registers
+        // Rows past the sequence end hold whatever the cache holds there; P is
+        // 0 for them, but 0 * NaN would still poison PV, so those V rows are 0.
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+            if (v_row[x] >= nvalid) vw[x][0] = vw[x][1] = vw[x][2] = vw[x][3] = 0u;
+
+        // ---- S^T = K . Q^T (permuted dims)
+        float s[NB][4];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+            uint32_t a[4];
+            e4m3x4_to_f16(kw[kb], a[0], a[2]);        // token gid
+            e4m3x4_to_f16(kw[8 + kb], a[1], a[3]);    // token gid + 8
+#pragma unroll
+            for (int j = 0; j < NB; ++j) Mma<__half>::run(s[j], a, qb[j][kb][0], qb[j][kb][1]);
+        }
+
+        float al[NB][2];
+        uint32_t bh[NB][2], bl[NB][2];
+        if (softmax_tile<__half, NB>(s, csc, vis, nvalid, stage_tok, r0 + gid, r0 + gid + 8, m, l,
+                                     al, bh, bl))
+            rescale_acc<NB>(acc, al);
+
+        // ---- O^T += V^T . P^T (permuted dims)
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+            // bytes 2mb, 2mb+1 of tokens (2tig, 2tig+1) and (2tig+8, 2tig+9), interleaved
+            const uint32_t sel = (mb & 1) ? 0x7362u : 0x5140u;
+            uint32_t a[4];
+            e4m3x4_to_f16(__byte_perm(vw[0][mb >> 1], vw[1][mb >> 1], sel), a[0], a[1]);
+            e4m3x4_to_f16(__byte_perm(vw[2][mb >> 1], vw[3][mb >> 1], sel), a[2], a[3]);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                Mma<__half>::run(acc[mb][j], a, bh[j][0], bh[j][1]);
+                Mma<__half>::run(acc[mb][j], a, bl[j][0], bl[j][1]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) l[j][e] += __shfl_xor_sync(kFull, l[j][e], o);
+
+    named_sync(1, kConsumerWarps * 32);
+    if (*c.cons_abort) return false;   // states are not written after a timeout
+    float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
+    float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
+    float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int col = 8 * j + 2 * tig + e;
+            if (gid == 0) {
+                wm[cw * kCols + col] = m[j][e];
+                wl[cw * kCols + col] = l[j][e];
+            }
+#pragma unroll
+            for (int mb = 0; mb < 8; ++mb)
+                *reinterpret_cast<float2*>(wacc + (cw * kCols + col) * kHeadDim + 16 * gid + 2 * mb) =
+                    make_float2(acc[mb][j][e], acc[mb][j][e + 2]);
+        }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// The split kernel.  The consumer is consume_tc<T, NB> (default), consume_f8<T, NB> or
 // consume_simt<T, G>; both leave per-warp states of up to 16 columns for the
 // final merge.
 // ---------------------------------------------------------------------------
@@ -773,16 +948,16 @@ struct Consumer;
 // KIND 1, 2: tensor cores with 8 or 16 columns; 21, 22: the same on an fp8
 // cache; KIND 10 + G: CUDA cores, group G
 template <typename T> struct Consumer<T, 1> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1, false>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 2> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2, false>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 21> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 1, true>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 1>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 22> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2, true>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 2>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 11> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 1>(c, w, l); }

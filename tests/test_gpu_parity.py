@@ -566,3 +566,61 @@ def test_fp8_long_gqa_128k_one_layer():
     ref_o, ref_l = oracle_all(q, k8, v8, sl, c["dtype"], Hkv, kv_dtype="e4m3",
                               k_scale=1 / g, v_scale=1 / g)
     assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 long_gqa_128k S={S}")
+
+
+@fp8_only
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+def test_fp8_every_finite_code(q_dtype):
+    """Every finite E4M3 pattern (254 of them: both zeros, subnormals, +-448)
+    occurs in K and in V, so each one goes through the kernel's conversion;
+    a ragged length puts NaN patterns in the tail that must stay unseen."""
+    B, Hkv, G, D, T = 1, 1, 8, 128, 1016
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    rng = np.random.default_rng(2100)
+    cells = T * D
+    k_raw = rng.permutation(np.resize(codes, cells)).reshape(B, Hkv, T, D)
+    v_raw = rng.permutation(np.resize(codes, cells)).reshape(B, Hkv, T, D)
+    k8 = torch.from_numpy(k_raw.copy()).view(torch.float8_e4m3fn).to(DEV)
+    v8 = torch.from_numpy(v_raw.copy()).view(torch.float8_e4m3fn).to(DEV)
+    lens = [1001]
+    _nan_past_lengths_fp8(k8, lens)
+    _nan_past_lengths_fp8(v8, lens)
+    q = fd_inputs.randn((B, Hkv * G, D), q_dtype, 2101, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    sc = dict(k_scale=1 / 64, v_scale=1 / 64)
+    ref_o, ref_l = oracle_all(q, k8, v8, sl, q_dtype, Hkv, kv_dtype="e4m3", **sc)
+    for S in (0, 4):
+        got_o, got_l, _ = run_decode(q, k8, v8, sl, n_splits=S, **sc)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 every code q={q_dtype} S={S}")
+
+
+@fp8_only
+@pytest.mark.parametrize("case", ["small", "large"])
+def test_fp8_bf16_query_magnitudes(case):
+    """bf16 query heads of very different magnitudes against an fp8 cache:
+    a zero head, heads near the bottom of the bf16 range, heads far above the
+    f16 range (with a tiny k_scale so that their scores stay moderate), and a
+    head whose dims differ by 2^20 among themselves."""
+    B, Hkv, G, D, T = 2, 2, 4, 128, 1500
+    Hq = Hkv * G
+    base = fd_inputs.randn((B, Hq, D), "f32", 2200, device="cpu")
+    if case == "small":
+        heads = [1.0, 2.0 ** -8, 2.0 ** 4, 0.0, 2.0 ** -120, None, 2.0 ** -30, 1.0]
+        k_scale = 1 / GAIN_K
+    else:
+        heads = [2.0 ** 20, 2.0 ** 16, 2.0 ** 18, 1.0, 2.0 ** 20, None, 2.0 ** -4, 2.0 ** 19]
+        k_scale = 2.0 ** -20 / GAIN_K
+    for h, f in enumerate(heads):
+        if f is None:                    # dims 64.. are 2^-20 of dims ..63
+            base[:, h, 64:] *= 2.0 ** -20
+        else:
+            base[:, h] *= f
+    q = base.to(torch.bfloat16).to(DEV)
+    k8 = fd_inputs.randn_fp8((B, Hkv, T, D), 2210, device=DEV, gain=GAIN_K)
+    v8 = fd_inputs.randn_fp8((B, Hkv, T, D), 2211, device=DEV, gain=GAIN_V)
+    sl = np.array([1500, 777], dtype=np.int32)
+    sc = dict(k_scale=k_scale, v_scale=1 / GAIN_V)
+    ref_o, ref_l = oracle_all(q, k8, v8, sl, "bf16", Hkv, kv_dtype="e4m3", **sc)
+    for S in (0, 6):
+        got_o, got_l, _ = run_decode(q, k8, v8, sl, n_splits=S, **sc)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 bf16 q magnitudes {case} S={S}")
