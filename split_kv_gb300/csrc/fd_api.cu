@@ -143,8 +143,9 @@ fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t
     const bool paged = d->page_size > 0;
     const int64_t n_tok = paged ? d->page_size : d->kv_extent;
     const int64_t n_outer = paged ? d->kv_extent : (d->batch > 0 ? d->batch : 1);
+    const int cols = (d->n_q_heads / d->n_kv_heads) * q_len_of(d);
     const int rows = paged ? (d->page_size < fdk::kPagedBoxRows ? d->page_size : fdk::kPagedBoxRows)
-                           : fdk::kSub;
+                           : fdk::stage_tokens(is_fp8(d), cols);
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(n_tok),
                           static_cast<cuuint64_t>(d->n_kv_heads), static_cast<cuuint64_t>(n_outer)};
     // byte strides of dims 1..3; a stride of a size-1 dim is never used, but

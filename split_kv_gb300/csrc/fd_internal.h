@@ -17,6 +17,13 @@ constexpr int kHalfBytes = kSub * 128;                // one [kSub tokens x 64 d
 constexpr int kSplitUnit = 16;                        // split ranges are whole 16-token units
 constexpr int kPagedBoxRows = 16;                     // paged boxes: at most one unit of one page
 constexpr int kStageBytes = 4 * kHalfBytes;           // K lo, K hi, V lo, V hi
+// fp8 caches with at most 8 columns per CTA: six consumer warps, 96-token stages
+constexpr int kConsumerWarpsF8 = 6;
+constexpr int kSubF8 = 16 * kConsumerWarpsF8;
+
+// Tokens per pipeline stage (the height of a contiguous cache's TMA box) of
+// the split-kernel variant that serves `cols` columns per CTA.
+inline int stage_tokens(bool fp8, int cols) { return fp8 && cols <= 8 ? kSubF8 : kSub; }
 
 // Device status bits (sticky until fd_device_status(clear)).
 constexpr unsigned kStatusTimeoutBit = 1u;   // an mbarrier wait ran past its limit
@@ -58,8 +65,6 @@ struct CombineParams {
     int32_t n_splits;
     int32_t out_dtype;              // 0 f16, 1 bf16, 2 f32
 };
-
-size_t split_smem_bytes(bool fp8);
 
 // Launches `kern` with programmatic stream serialization, so that it may
 // start while the previous kernel in the stream finishes; the kernel itself

@@ -147,21 +147,33 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 
 }  // namespace
 
-// Map of the fp8-cache variant: 6 stages of [64 tokens x 128 dims] e4m3 K and
-// V boxes (16 KB each stage, the same bytes in flight as the 16-bit ring),
-// then the barriers.  Consumers read a stage straight into registers.
-constexpr int kStagesF8 = 6;
-constexpr int kTileBytesF8 = kSub * 128;                          // one e4m3 box: 64 rows x 128 B
-constexpr int kStageBytesF8 = 2 * kTileBytesF8;                   // K, V
-constexpr int kOffBarsF8 = kStagesF8 * kStageBytesF8;             // full[6], empty[6]
-constexpr int kOffFlagF8 = kOffBarsF8 + 128;
-constexpr int kSmemUsedF8 = kOffFlagF8 + 16;
-static_assert(2 * kStagesF8 * 8 <= 128, "barriers must fit");
-static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBarsF8, "merge area must fit");
-
-size_t split_smem_bytes(bool fp8) {
-    return static_cast<size_t>(fp8 ? kSmemUsedF8 : kSmemUsed) + 1024;
-}
+// Geometry of each kernel variant (KIND, see Consumer below).  16-bit caches:
+// four consumer warps, 3 stages of 64 tokens, each stage four [64 x 64-dim]
+// boxes (the map above).  fp8 caches: two [rows x 128-dim] e4m3 boxes (K, V)
+// per stage, read by the consumers straight into registers; with at most 8
+// columns per CTA (KIND 21) six consumer warps take 96-token stages, 4 deep,
+// otherwise (KIND 22) four take 64-token stages, 6 deep.  Either way the ring
+// holds 96 KB, and two CTAs fit on an SM.
+template <int KIND>
+struct Geo {
+    static constexpr bool kF8 = KIND >= 20;
+    static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kConsumerWarps;
+    static constexpr int kSub = 16 * kWarps;                   // tokens per stage
+    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kStages;
+    static constexpr int kTile = kSub * 128;                   // one box of 128-byte rows
+    static constexpr int kStageBytes = (kF8 ? 2 : 4) * kTile;
+    static constexpr int kOffBars = kRing * kStageBytes;       // full[kRing], empty[kRing]
+    static constexpr int kOffFlag = (kF8 ? kOffBars + 128 : fdk::kOffFlag);
+    static constexpr int kSmem = (kF8 ? kOffFlag + 16 : kSmemUsed) + 1024;   // + alignment slack
+    static constexpr int kThreads = (kWarps + 1) * 32;         // + one TMA producer warp
+    // end-of-split merge area in stage memory: acc [warps][16][128], m, l [warps][16]
+    static constexpr int kOffWM = kWarps * kCols * kHeadDim * 4;
+    static constexpr int kOffWL = kOffWM + kWarps * kCols * 4;
+    static_assert(2 * kRing * 8 <= 128, "barriers must fit");
+    static_assert(kOffWL + kWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
+    static_assert(kF8 || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
+                          kOffBars == fdk::kOffBars), "16-bit variants use the map above");
+};
 
 // Everything a CTA knows about its split, shared by the producer and consumers.
 struct SplitCtx {
@@ -185,11 +197,14 @@ struct SplitCtx {
 // [rows x 64 dims] boxes per stage (K, V low and high halves); fp8 caches
 // (F8): two [rows x 128 dims] boxes (K, V).
 // ---------------------------------------------------------------------------
-template <bool F8>
+template <int KIND>
 __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tmK,
                                         const CUtensorMap* tmV, int lane) {
-    constexpr int kStages = F8 ? kStagesF8 : fdk::kStages;
-    constexpr int kStageBytes = F8 ? kStageBytesF8 : fdk::kStageBytes;
+    using Gm = Geo<KIND>;
+    constexpr bool F8 = Gm::kF8;
+    constexpr int kStages = Gm::kRing;
+    constexpr int kStageBytes = Gm::kStageBytes;
+    constexpr int kSub = Gm::kSub;
     const SplitParams& p = *c.p;
     const uint64_t policy = policy_evict_first();
     const bool paged = p.page_size != 0;
@@ -234,7 +249,7 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
                 const int outer = paged ? page : c.b;
                 const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
                 tma_load_4d_hint(dst + off, tmK, bar, 0, row, c.kvh, outer, policy);
-                tma_load_4d_hint(dst + kTileBytesF8 + off, tmV, bar, 0, row, c.kvh, outer, policy);
+                tma_load_4d_hint(dst + Gm::kTile + off, tmV, bar, 0, row, c.kvh, outer, policy);
             }
         } else if (!paged) {
             if (lane == 0) {
@@ -495,52 +510,77 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Online softmax (base 2) of one 16-token tile for up to 8 * NB columns, and
-// P^T as hi + lo B fragments of the PV MMAs.  s holds S^T (C fragments);
-// csc[j][e] is the base-2 score scale of the lane's column 8j + 2tig + e;
-// a column sees the keys before vis[j][e] and the stage's first nvalid rows.
+// Online softmax (base 2) of TILES 16-token tiles for up to 8 * NB columns,
+// and P^T of each tile as hi + lo B fragments of the PV MMAs.  s[t] holds tile
+// t's S^T (C fragments); csc[j][e] is the base-2 score scale of the lane's
+// column 8j + 2tig + e, which sees the keys before vis[j][e]; tile t starts at
+// key tok[t] and has nvalid[t] rows.  Without `masked` every row is taken as
+// visible to every column (a full tile and one query per sequence).  The
+// running max moves once per call.
 // Returns whether any running max moved (the accumulators then take al).
-template <typename MT, int NB>
-__device__ __forceinline__ bool softmax_tile(const float (&s)[NB][4], const float (&csc)[NB][2],
-                                             const int (&vis)[NB][2], int nvalid, int stage_tok,
-                                             int row0, int row1, float (&m)[NB][2],
-                                             float (&l)[NB][2], float (&al)[NB][2],
-                                             uint32_t (&bh)[NB][2], uint32_t (&bl)[NB][2]) {
+template <typename MT, int NB, int TILES>
+__device__ __forceinline__ bool softmax_tiles(const float (&s)[TILES][NB][4], const float (&csc)[NB][2],
+                                              const int (&vis)[NB][2], const int (&nvalid)[TILES],
+                                              const int (&tok)[TILES], int row0, int row1,
+                                              bool masked, float (&m)[NB][2], float (&l)[NB][2],
+                                              float (&al)[NB][2], uint32_t (&bh)[TILES][NB][2],
+                                              uint32_t (&bl)[TILES][NB][2]) {
     bool rescale = false;
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-        float t[4];
+        float t[TILES][4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int lim = min(nvalid, vis[j][e] - stage_tok);
-            t[e] = row0 < lim ? s[j][e] * csc[j][e] : -INFINITY;         // token gid
-            t[e + 2] = row1 < lim ? s[j][e + 2] * csc[j][e] : -INFINITY; // token gid + 8
+        for (int x = 0; x < TILES; ++x)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                t[x][e] = s[x][j][e] * csc[j][e];           // token gid
+                t[x][e + 2] = s[x][j][e + 2] * csc[j][e];   // token gid + 8
+            }
+        if (masked) {   // warp-uniform: a partial tile, or columns with their own prefix
+#pragma unroll
+            for (int x = 0; x < TILES; ++x)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int lim = min(nvalid[x], vis[j][e] - tok[x]);
+                    if (row0 >= lim) t[x][e] = -INFINITY;
+                    if (row1 >= lim) t[x][e + 2] = -INFINITY;
+                }
         }
-        float pr[4];
+        float pr[TILES][4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(t[e], t[e + 2]);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < TILES; ++x) mx = fmaxf(mx, fmaxf(t[x][e], t[x][e + 2]));
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
             const float mn = fmaxf(m[j][e], mx);
             const float mu = mn == -INFINITY ? 0.f : mn;   // never -inf - -inf
             al[j][e] = fast_exp2(m[j][e] - mu);
-            pr[e] = fast_exp2(t[e] - mu);
-            pr[e + 2] = fast_exp2(t[e + 2] - mu);
-            l[j][e] = fmaf(al[j][e], l[j][e], pr[e] + pr[e + 2]);
+            float sum = 0.f;
+#pragma unroll
+            for (int x = 0; x < TILES; ++x) {
+                pr[x][e] = fast_exp2(t[x][e] - mu);
+                pr[x][e + 2] = fast_exp2(t[x][e + 2] - mu);
+                sum += pr[x][e] + pr[x][e + 2];
+            }
+            l[j][e] = fmaf(al[j][e], l[j][e], sum);
             m[j][e] = mn;
             rescale |= al[j][e] != 1.f;
         }
         // P^T as B fragments: hi + lo parts, transposed in registers
-        float k0, k1, k2, k3, d0, d1, d2, d3;
-        const uint32_t hi01 = Mma<MT>::pack(pr[0], pr[1], k0, k1);
-        const uint32_t hi23 = Mma<MT>::pack(pr[2], pr[3], k2, k3);
-        const uint32_t lo01 = Mma<MT>::pack(pr[0] - k0, pr[1] - k1, d0, d1);
-        const uint32_t lo23 = Mma<MT>::pack(pr[2] - k2, pr[3] - k3, d2, d3);
-        bh[j][0] = movmatrix_trans(hi01);
-        bh[j][1] = movmatrix_trans(hi23);
-        bl[j][0] = movmatrix_trans(lo01);
-        bl[j][1] = movmatrix_trans(lo23);
+#pragma unroll
+        for (int x = 0; x < TILES; ++x) {
+            float k0, k1, k2, k3, d0, d1, d2, d3;
+            const uint32_t hi01 = Mma<MT>::pack(pr[x][0], pr[x][1], k0, k1);
+            const uint32_t hi23 = Mma<MT>::pack(pr[x][2], pr[x][3], k2, k3);
+            const uint32_t lo01 = Mma<MT>::pack(pr[x][0] - k0, pr[x][1] - k1, d0, d1);
+            const uint32_t lo23 = Mma<MT>::pack(pr[x][2] - k2, pr[x][3] - k3, d2, d3);
+            bh[x][j][0] = movmatrix_trans(hi01);
+            bh[x][j][1] = movmatrix_trans(hi23);
+            bl[x][j][0] = movmatrix_trans(lo01);
+            bl[x][j][1] = movmatrix_trans(lo23);
+        }
     }
     return __any_sync(kFull, rescale);
 }
@@ -661,9 +701,9 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
         }
 
         // ---- S^T = K . Q^T for the warp's 16 tokens
-        float s[NB][4];
+        float s[1][NB][4];
 #pragma unroll
-        for (int j = 0; j < NB; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int j = 0; j < NB; ++j) s[0][j][0] = s[0][j][1] = s[0][j][2] = s[0][j][3] = 0.f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             const int chunk = 2 * kb + k_csel;                     // 16-byte chunk of the row
@@ -672,14 +712,16 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             uint32_t a[4];
             ldsm_x4(a, addr);
 #pragma unroll
-            for (int j = 0; j < NB; ++j) Mma<T>::run(s[j], a, qb[j][kb][0], qb[j][kb][1]);
+            for (int j = 0; j < NB; ++j) Mma<T>::run(s[0][j], a, qb[j][kb][0], qb[j][kb][1]);
         }
 
         // ---- online softmax per column over the 16 tokens
         float al[NB][2];
-        uint32_t bh[NB][2], bl[NB][2];
-        if (softmax_tile<T, NB>(s, csc, vis, nvalid, stage_tok, r0 + gid, r0 + gid + 8, m, l, al,
-                                bh, bl))
+        uint32_t bh[1][NB][2], bl[1][NB][2];
+        const int nv[1] = {nvalid}, tk[1] = {stage_tok};
+        if (softmax_tiles<T, NB, 1>(s, csc, vis, nv, tk, r0 + gid, r0 + gid + 8,
+                                    nvalid < kSub || stage_tok + kSub > c.L - p.q_len + 1, m, l,
+                                    al, bh, bl))
             rescale_acc<NB>(acc, al);
 
         // ---- O^T += V^T . P^T
@@ -692,8 +734,8 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
             ldsm_x4_trans(a, addr);
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
-                Mma<T>::run(acc[mb][j], a, bh[j][0], bh[j][1]);
-                Mma<T>::run(acc[mb][j], a, bl[j][0], bl[j][1]);
+                Mma<T>::run(acc[mb][j], a, bh[0][j][0], bh[0][j][1]);
+                Mma<T>::run(acc[mb][j], a, bl[0][j][0], bl[0][j][1]);
             }
         }
         __syncwarp();
@@ -748,7 +790,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 // (every element within 2^31 of it converts exactly); that column's score
 // scale takes the inverse power.  P goes to f16 as hi + lo parts.
 // The warp's 8 chunk loads are its only reads of a stage, so it hands the
-// stage back to the producer right after them.
+// stage back to the producer right after them.  An e4m3 stage carries half
+// the bytes of a 16-bit one, so the same arithmetic per token has half the
+// time: the narrow variant (KIND 21) runs six consumer warps per CTA to hide
+// the instruction latencies that bound this consumer.
 // ---------------------------------------------------------------------------
 // four e4m3 bytes -> two f16 pairs: (b0, b1) and (b2, b3), low byte in the low half
 __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -762,8 +807,12 @@ __device__ __forceinline__ void unpack4(const uint4& r, uint32_t* w) {
     w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
 }
 
-template <typename T, int NB>
+template <typename T, int KIND>
 __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) {
+    using Gm = Geo<KIND>;
+    constexpr int NB = KIND == 21 ? 1 : 2;
+    constexpr int kSub = Gm::kSub;
+    constexpr int kRing = Gm::kRing;
     const SplitParams& p = *c.p;
     const int gid = lane >> 2, tig = lane & 3;
     const int r0 = cw * 16;                      // the warp's 16 rows of each stage
@@ -843,21 +892,21 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         v_row[x] = r0 + 2 * tig + (x & 1) + (x >> 1) * 8;
-        v_off[x] = kTileBytesF8 + v_row[x] * 128 + ((gid ^ (v_row[x] & 7)) << 4);
+        v_off[x] = Gm::kTile + v_row[x] * 128 + ((gid ^ (v_row[x] & 7)) << 4);
     }
 
 #pragma unroll 1
     for (int it = 0; it < c.n_sub; ++it) {
-        const int st = it % kStagesF8;
-        const bool ok = wait_or_flag(c.full_bar(st), (it / kStagesF8) & 1);
+        const int st = it % kRing;
+        const bool ok = wait_or_flag(c.full_bar(st), (it / kRing) & 1);
         if (!__all_sync(kFull, ok)) {
             *c.cons_abort = 1;
             *c.abort_flag = 1;
             break;
         }
-        const uint8_t* sb = c.smem + st * kStageBytesF8;
-        const int stage_tok = c.tok0 + it * kSub;
-        const int nvalid = min(kSub, c.tok1 - stage_tok);
+        const uint8_t* sb = c.smem + st * Gm::kStageBytes;
+        const int tok = c.tok0 + it * kSub;
+        const int nvalid = min(kSub, c.tok1 - tok);
 
         uint32_t kw[16], vw[4][4];
         unpack4(*reinterpret_cast<const uint4*>(sb + k_off0), kw);
@@ -868,29 +917,46 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
         for (int x = 0; x < 4; ++x) unpack4(*reinterpret_cast<const uint4*>(sb + v_off[x]), vw[x]);
         __syncwarp();
         if (lane == 0) mbar_arrive(c.empty_bar(st));   // the stage is in registers
-        // Rows past the sequence end hold whatever the cache holds there; P is
-        // 0 for them, but 0 * NaN would still poison PV, so those V rows are 0.
+        const bool partial = nvalid < kSub;            // the split's last stage
+        if (partial) {
+            // Rows past the end hold whatever the cache holds there; P is 0 for
+            // them, but 0 * NaN would still poison PV, so those V rows are 0.
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
-            if (v_row[x] >= nvalid) vw[x][0] = vw[x][1] = vw[x][2] = vw[x][3] = 0u;
+            for (int x = 0; x < 4; ++x)
+                if (v_row[x] >= nvalid) vw[x][0] = vw[x][1] = vw[x][2] = vw[x][3] = 0u;
+        }
 
-        // ---- S^T = K . Q^T (permuted dims)
-        float s[NB][4];
+        // ---- S^T = K . Q^T (permuted dims); with one N block, even and odd k
+        // blocks go to separate accumulators: two MMA chains of four
+        constexpr bool kTwoChains = NB == 1;
+        float s[1][NB][4], s2[NB][4];
 #pragma unroll
-        for (int j = 0; j < NB; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int j = 0; j < NB; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[0][j][e] = s2[j][e] = 0.f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
             uint32_t a[4];
             e4m3x4_to_f16(kw[kb], a[0], a[2]);        // token gid
             e4m3x4_to_f16(kw[8 + kb], a[1], a[3]);    // token gid + 8
 #pragma unroll
-            for (int j = 0; j < NB; ++j) Mma<__half>::run(s[j], a, qb[j][kb][0], qb[j][kb][1]);
+            for (int j = 0; j < NB; ++j)
+                Mma<__half>::run((kTwoChains && (kb & 1)) ? s2[j] : s[0][j], a, qb[j][kb][0],
+                                 qb[j][kb][1]);
+        }
+        if constexpr (kTwoChains) {
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[0][j][e] += s2[j][e];
         }
 
         float al[NB][2];
-        uint32_t bh[NB][2], bl[NB][2];
-        if (softmax_tile<__half, NB>(s, csc, vis, nvalid, stage_tok, r0 + gid, r0 + gid + 8, m, l,
-                                     al, bh, bl))
+        uint32_t bh[1][NB][2], bl[1][NB][2];
+        const int nv[1] = {nvalid}, tk[1] = {tok};
+        if (softmax_tiles<__half, NB, 1>(s, csc, vis, nv, tk, r0 + gid, r0 + gid + 8,
+                                         partial || tok + kSub > c.L - p.q_len + 1, m, l, al, bh,
+                                         bl))
             rescale_acc<NB>(acc, al);
 
         // ---- O^T += V^T . P^T (permuted dims)
@@ -903,8 +969,8 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
             e4m3x4_to_f16(__byte_perm(vw[2][mb >> 1], vw[3][mb >> 1], sel), a[2], a[3]);
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
-                Mma<__half>::run(acc[mb][j], a, bh[j][0], bh[j][1]);
-                Mma<__half>::run(acc[mb][j], a, bl[j][0], bl[j][1]);
+                Mma<__half>::run(acc[mb][j], a, bh[0][j][0], bh[0][j][1]);
+                Mma<__half>::run(acc[mb][j], a, bl[0][j][0], bl[0][j][1]);
             }
         }
     }
@@ -916,11 +982,11 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) l[j][e] += __shfl_xor_sync(kFull, l[j][e], o);
 
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, Gm::kWarps * 32);
     if (*c.cons_abort) return false;   // states are not written after a timeout
-    float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
-    float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
-    float* wl = reinterpret_cast<float*>(c.smem + kOffWL);
+    float* wacc = reinterpret_cast<float*>(c.smem);
+    float* wm = reinterpret_cast<float*>(c.smem + Gm::kOffWM);
+    float* wl = reinterpret_cast<float*>(c.smem + Gm::kOffWL);
 #pragma unroll
     for (int j = 0; j < NB; ++j)
 #pragma unroll
@@ -939,7 +1005,7 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
 }
 
 // ---------------------------------------------------------------------------
-// The split kernel.  The consumer is consume_tc<T, NB> (default), consume_f8<T, NB> or
+// The split kernel.  The consumer is consume_tc<T, NB> (default), consume_f8<T, KIND> or
 // consume_simt<T, G>; both leave per-warp states of up to 16 columns for the
 // final merge.
 // ---------------------------------------------------------------------------
@@ -954,10 +1020,10 @@ template <typename T> struct Consumer<T, 2> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_tc<T, 2>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 21> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 1>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 21>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 22> {
-    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 2>(c, w, l); }
+    static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_f8<T, 22>(c, w, l); }
 };
 template <typename T> struct Consumer<T, 11> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 1>(c, w, l); }
@@ -973,11 +1039,12 @@ template <typename T> struct Consumer<T, 18> {
 };
 
 template <typename T, int KIND>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    constexpr bool F8 = KIND >= 20;
-    constexpr int kRing = F8 ? kStagesF8 : kStages;
+    using Gm = Geo<KIND>;
+    constexpr int kRing = Gm::kRing;
+    constexpr int kWarps = Gm::kWarps;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -994,20 +1061,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
 
-    c.bar0 = smem_u32(smem + (F8 ? kOffBarsF8 : kOffBars));
-    c.abort_flag = reinterpret_cast<volatile int*>(smem + (F8 ? kOffFlagF8 : kOffFlag));
-    c.cons_abort = reinterpret_cast<volatile int*>(smem + (F8 ? kOffFlagF8 : kOffFlag) + 4);
+    c.bar0 = smem_u32(smem + Gm::kOffBars);
+    c.abort_flag = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag);
+    c.cons_abort = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 4);
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < kRing; ++s) {
             mbar_init(c.full_bar(s), 1);
-            mbar_init(c.empty_bar(s), kConsumerWarps);
+            mbar_init(c.empty_bar(s), kWarps);
         }
         *c.abort_flag = 0;
         *c.cons_abort = 0;
         fence_barrier_init();
     }
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == kWarps && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
@@ -1033,31 +1100,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int u_count = base + (c.split < rem ? 1 : 0);
     c.tok0 = u_begin * unit;
     c.tok1 = min((u_begin + u_count) * unit, L);
-    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + kSub - 1) / kSub : 0;
+    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Gm::kSub - 1) / Gm::kSub : 0;
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
-        produce<F8>(c, &tmK, &tmV, lane);
+    if (warp == kWarps) {
+        produce<KIND>(c, &tmK, &tmV, lane);
         return;
     }
 
     if (!Consumer<T, KIND>::run(c, warp, lane)) return;
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, kWarps * 32);
+    if (threadIdx.x >= kHeadDim) return;   // one thread per dim below
 
-    // ---- merge the four warp states of each column and write the split's state
-    const float* wacc = reinterpret_cast<const float*>(smem + kOffWAcc);
-    const float* wm = reinterpret_cast<const float*>(smem + kOffWM);
-    const float* wl = reinterpret_cast<const float*>(smem + kOffWL);
+    // ---- merge the consumer warps' states of each column and write the split's state
+    const float* wacc = reinterpret_cast<const float*>(smem);
+    const float* wm = reinterpret_cast<const float*>(smem + Gm::kOffWM);
+    const float* wl = reinterpret_cast<const float*>(smem + Gm::kOffWL);
     const int d = threadIdx.x;   // 0 .. 127
     const int ncols = min(kCols, p.cols - c.cb * kCols);
     for (int col = 0; col < ncols; ++col) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * kCols + col]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kCols + col]);
         float u = 0.f, l = 0.f, m_out = -INFINITY;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
+            for (int w = 0; w < kWarps; ++w) {
                 const float mw = wm[w * kCols + col];
                 const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
                 u = fmaf(e, wacc[(w * kCols + col) * kHeadDim + d], u);
@@ -1083,7 +1151,7 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
     auto kern = fd_split_kernel<T, KIND>;
-    const size_t smem = split_smem_bytes(KIND >= 20);
+    const size_t smem = Geo<KIND>::kSmem;
     // one attribute call per (kernel, device): cheap and safe to repeat
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -1094,8 +1162,8 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads * p.col_blocks, batch), dim3(kThreads),
-                      smem, stream, tmK, tmV, p);
+    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads * p.col_blocks, batch),
+                      dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
 template <typename T>

@@ -396,17 +396,27 @@ def test_lse_chaining_two_halves_merged_externally():
     np.testing.assert_allclose(got_l, l_full, rtol=0, atol=2e-5)
 
 
-def test_bounded_wait_reports_timeout_and_the_context_survives():
+@pytest.mark.parametrize("kind", ["f16", "e4m3"])
+def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     """The test hook drops the first K/V stage: the kernel's bounded wait runs
     out, the status word reports FD_ERR_DEVICE_TIMEOUT, nothing faults, and
-    the next call on the same context is correct."""
+    the next call on the same context is correct.  Both the 16-bit consumer
+    and the fp8 one (which waits for two stages per iteration)."""
     import time
+    if kind == "e4m3" and not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
     B, Hq, Hkv, D, T = 1, 8, 8, 128, 300
     q = fd_inputs.randn((B, Hq, D), "f16", 1201, device=DEV)
-    k, v = _cache(B, Hkv, T, D, "f16", 1202)
+    sc = {}
+    if kind == "e4m3":
+        k = fd_inputs.randn_fp8((B, Hkv, T, D), 1203, device=DEV, gain=16.0)
+        v = fd_inputs.randn_fp8((B, Hkv, T, D), 1204, device=DEV, gain=16.0)
+        sc = dict(k_scale=1 / 16, v_scale=1 / 16)
+    else:
+        k, v = _cache(B, Hkv, T, D, "f16", 1202)
     sl_h = np.array([T], dtype=np.int32)
     seqlens = torch.from_numpy(sl_h).to(DEV)
-    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=1)
+    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=1, **sc)
     desc.flags = fd.FD_FLAG_TEST_DROP_FIRST_STAGE
     ws = torch.empty(fd.fd_workspace_size(desc, 1), dtype=torch.uint8, device=DEV)
     out = torch.zeros(B, Hq, D, dtype=torch.float32, device=DEV)
@@ -416,9 +426,10 @@ def test_bounded_wait_reports_timeout_and_the_context_survives():
     assert fd.fd_device_status(clear=True) == fd.FD_ERR_DEVICE_TIMEOUT
     assert time.time() - t0 < 60
     assert fd.fd_device_status(clear=True) == fd.FD_OK
-    got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1)
-    ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv)
-    assert_parity(got_o, got_l, ref_o, ref_l, "after a timed-out call")
+    got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1, **sc)
+    ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv, kv_dtype=kind if kind == "e4m3" else None,
+                              **sc)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"after a timed-out call ({kind})")
 
 
 def test_fd_decode_replays_from_a_cuda_graph():
