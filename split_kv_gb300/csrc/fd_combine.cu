@@ -27,10 +27,12 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;
 constexpr int kWarps = kHeadDim / 32;   // 4
+constexpr int kPre = 8;                 // splits per thread loaded up front (S <= 32: all)
 
 // One CTA (4 warps) per row.  Thread (w, lane) accumulates dims 4*lane..+3
 // over splits i = w, w+4, ..., so the row's S x 128 partial outputs are all
-// in flight at once; the four warp partials are added in a fixed order.
+// in flight at once (up to 32 splits together with m and l); the four warp
+// partials are added in a fixed order.
 __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParams p) {
     __shared__ float s_m[kMaxSplits], s_w[kMaxSplits], s_l[kMaxSplits];
     __shared__ float4 s_part[kWarps][32];
@@ -44,6 +46,15 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
     const int t = threadIdx.x;
     const int w = t >> 5, lane = t & 31;
     const int S = p.n_splits;
+    // The partial outputs do not depend on m and l: request the first kPre of
+    // this thread's splits now, so that they travel with m and l.
+    const float4* urow = reinterpret_cast<const float4*>(p.ws_u + static_cast<int64_t>(row) * S * kHeadDim) + lane;
+    float4 pre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int i = w + kWarps * k;
+        pre[k] = i < S ? urow[i * (kHeadDim / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (t < S) {
         s_m[t] = p.ws_m[static_cast<int64_t>(row) * S + t];
         s_l[t] = p.ws_l[static_cast<int64_t>(row) * S + t];
@@ -70,10 +81,20 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
     }
     __syncthreads();
 
-    const float4* urow = reinterpret_cast<const float4*>(p.ws_u + static_cast<int64_t>(row) * S * kHeadDim) + lane;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int i = w + kWarps * k;
+        if (i < S) {
+            const float wt = s_w[i];
+            a.x = fmaf(wt, pre[k].x, a.x);
+            a.y = fmaf(wt, pre[k].y, a.y);
+            a.z = fmaf(wt, pre[k].z, a.z);
+            a.w = fmaf(wt, pre[k].w, a.w);
+        }
+    }
 #pragma unroll 8
-    for (int i = w; i < S; i += kWarps) {
+    for (int i = w + kWarps * kPre; i < S; i += kWarps) {
         const float wt = s_w[i];
         const float4 u = urow[i * (kHeadDim / 4)];
         a.x = fmaf(wt, u.x, a.x);

@@ -400,6 +400,22 @@ def test_e4m3_conversion_all_patterns():
     assert np.nanmax(got) == 448.0
 
 
+def test_e4m3_conversion_closed_form():
+    """The E4M3 'fn' definition written out: sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal (2^-6 x m/8); S.1111.111
+    is NaN and there are no infinities, so S.1111.110 = 448 is the largest."""
+    for b in range(256):
+        sgn = -1.0 if b & 0x80 else 1.0
+        e, m = (b >> 3) & 0xF, b & 0x7
+        got = oracle.e4m3_to_double(b)
+        if e == 0xF and m == 0x7:
+            assert math.isnan(got), b
+            continue
+        want = sgn * (2.0 ** -6) * (m / 8.0) if e == 0 else sgn * 2.0 ** (e - 7) * (1.0 + m / 8.0)
+        assert got == want, (b, got, want)
+    assert oracle.e4m3_to_double(0x7E) == 448.0 and oracle.e4m3_to_double(0x01) == 2.0 ** -9
+
+
 def test_e4m3_cache_with_scales_against_scipy():
     torch = pytest.importorskip("torch")
     if not hasattr(torch, "float8_e4m3fn"):
