@@ -636,7 +636,8 @@ def run_suite(args):
                 if rc != 0:
                     raise fd.FdError(rc, "fd_decode")
 
-            iters = max(20, min(400, int(2e9 / max(kv_bytes, 1))))
+            # at least 50 calls (several ms of timed work even for the smallest problems)
+            iters = max(50, min(2000, int(1e10 / max(kv_bytes, 1))))
             ms, note = _time_calls(call, n_sets, iters, max(3, args.warmup), stream, dev, args.eager)
             results[label] = (S, ms)
         fd.check(fd.fd_device_status(stream), "device status")

@@ -12,17 +12,19 @@
 // ragged batches).
 //
 // GB300 structure
-//  - Warp 4 is a TMA producer: per 64-token stage it issues four 2-D boxes
-//    [64 tokens x 64 dims] (K low/high half, V low/high half) with 128-byte
-//    swizzle into a 3-stage ring, completing on the stage's "full" mbarrier.
-//    Contiguous caches use one box per half; paged caches 16-row boxes (8 for
-//    8-token pages) resolved through the block table a stage ahead.
-//  - Warps 0-3 consume.  Each warp owns 16 of a stage's 64 rows and keeps its
-//    own running (m, l, acc) per query head; the four warp states are merged
-//    exactly at the end of the split (the same max-subtracted rule).
-//    QK: a half-warp covers one 256-byte K row (16 lanes x 8 dims) and the G
-//    partial dot products are reduced with a reduce-scatter butterfly (each
-//    lane ends with one head's score).  PV: each lane owns 4 dims x G heads.
+//  - The last warp is a TMA producer.  16-bit caches: per 64-token stage it
+//    issues four 2-D boxes [64 tokens x 64 dims] (K low/high half, V low/high
+//    half) with 128-byte swizzle into a 3-stage ring, completing on the
+//    stage's "full" mbarrier.  fp8 caches: two boxes of 128-byte rows (K, V)
+//    per stage.  Contiguous caches use one box per tensor (or half); paged
+//    caches 16-row boxes (8 for 8-token pages) resolved through the block
+//    table a stage ahead.  Geo<KIND> below holds each variant's geometry.
+//  - The other warps consume.  Each owns 16 of a stage's rows and keeps its
+//    own running (m, l, acc) per column; the warp states are merged exactly at
+//    the end of the split (the same max-subtracted rule).  Three consumers:
+//    consume_tc (default) runs QK^T and PV as warp MMAs fed by ldmatrix;
+//    consume_f8 builds the same MMAs' fragments from e4m3 bytes in registers;
+//    consume_simt (FD_FLAG_CUDA_CORES) uses FP32 FMAs, a half-warp per K row.
 //  - Scores are kept in base 2: t = (q.k) * log2(e)/sqrt(D), p = 2^(t - m).
 //    The workspace m is converted back to natural units of s.
 //  - Every mbarrier wait is bounded (2 s of wall time); on timeout the kernel
