@@ -61,17 +61,15 @@
 extern "C" {
 #endif
 
-#define FD_ABI_VERSION 4
+#define FD_ABI_VERSION 3
 #define FD_MAX_SPLITS 128   /* the split-count heuristic's cap ("Flash-Decoding ...", §6) */
 #define FD_TILE_TOKENS 128  /* split ranges are whole 128-token tiles; the planner's KV block */
-#define FD_TICKETS 16384    /* fused-combine tickets at the start of every workspace (uint32) */
 
 typedef enum fd_status {
     FD_OK = 0,
     FD_ERR_INVALID_ARG = -1,      /* null pointer, bad size/stride, inconsistent shape */
     FD_ERR_UNSUPPORTED = -2,      /* valid but not implemented (head_dim, G, dtype, page size) */
-    FD_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned; or (device status
-                                     word) a fused call found its ticket section not zeroed */
+    FD_ERR_WORKSPACE = -3,        /* workspace missing, too small or misaligned */
     FD_ERR_CUDA = -4,             /* a CUDA runtime / launch error */
     FD_ERR_DEVICE_TIMEOUT = -5,   /* a kernel wait ran past its limit (device status word) */
     FD_ERR_DEVICE_BOUNDS = -6     /* a seqlen or block-table entry was out of range (device status word) */
@@ -89,21 +87,6 @@ typedef enum fd_dtype { FD_F16 = 0, FD_BF16 = 1, FD_F32 = 2, FD_E4M3 = 3 } fd_dt
  * same memory pipeline, same results within the stated tolerance; kept for
  * comparison and profiling. */
 #define FD_FLAG_CUDA_CORES 1
-/* Fused combine for fd_decode and fd_decode_static ("Flash-Decoding ...",
- * §7 and §9: the last CTA to finish merges, no second launch): each split CTA
- * takes an arrival ticket after writing its states, and the CTA holding the
- * last ticket of its (sequence, KV head, column block) group merges that
- * group's rows into out / lse with the same arithmetic as fd_combine_states
- * (the results are bitwise those of the two-kernel path).  It needs the
- * workspace's ticket section (its first FD_TICKETS * 4 bytes) to hold zeros
- * before the call: call fd_workspace_init once on a new workspace (or
- * allocate it zeroed).  Every call, fused or not, leaves the section as it
- * found it, so one initialisation serves all later calls of any shape; a
- * call that finds a ticket not zero records FD_ERR_WORKSPACE in the device
- * status word (out and lse are then unspecified).  At most FD_TICKETS groups
- * (batch * n_kv_heads * ceil(G*q_len/16), 1 when G*q_len <= 8), else
- * FD_ERR_UNSUPPORTED.  fd_split_states ignores the flag. */
-#define FD_FLAG_FUSED_COMBINE (1 << 1)
 /* Test hook for failure detection, never for production: the split kernel
  * does not request its first K/V stage, so the wait for it runs out after its
  * limit (about 2 s), the kernel records FD_ERR_DEVICE_TIMEOUT in the device
@@ -189,10 +172,9 @@ int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t he
                 const int32_t* seqlens_host, int32_t num_sms);
 
 /* Bytes of workspace fd_decode needs for `n_splits` (<= 0: the split count
- * fd_decode would plan).  Layout (each section 256-byte aligned,
+ * fd_decode would plan).  Layout (all fp32, each section 256-byte aligned,
  * row r = (b*q_len + i)*n_q_heads + h):
- *     tickets [FD_TICKETS] uint32     fused-combine arrival tickets (0 between calls)
- *     u  [rows][n_splits][head_dim]   unnormalised partial outputs (fp32)
+ *     u  [rows][n_splits][head_dim]   unnormalised partial outputs
  *     m  [rows][n_splits]             max score of the split (natural units of s)
  *     l  [rows][n_splits]             sum of exp(s - m) over the split
  * with rows = batch*q_len*n_q_heads.
@@ -200,14 +182,7 @@ int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t he
  * descriptor. */
 size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits);
 
-/* Zeroes the ticket section of a workspace (an asynchronous memset of its
- * first FD_TICKETS * 4 bytes on `stream`), which FD_FLAG_FUSED_COMBINE needs
- * once before the workspace's first fused call.  FD_ERR_WORKSPACE for a null,
- * misaligned or too small workspace; FD_ERR_CUDA if the memset fails. */
-fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
-
-/* The whole decode step: fd_split_states then fd_combine_states on `stream`
- * (or, with FD_FLAG_FUSED_COMBINE, the split kernel alone, merging as it ends).
+/* The whole decode step: fd_split_states then fd_combine_states on `stream`.
  *  q, k_cache, v_cache : device, layouts in fd_desc.
  *  seqlens             : device int32[batch], 0 <= seqlens[b] <= capacity,
  *                        capacity = kv_extent (contiguous) or
@@ -218,8 +193,7 @@ fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* strea
  *                        scaled scores; NULL to skip.  A row with seqlens[b] = 0
  *                        gets out = 0 and lse = -inf.
  *  workspace           : device, >= fd_workspace_size(desc, n_splits) bytes,
- *                        256-byte aligned; contents on entry are ignored
- *                        except the ticket section (FD_FLAG_FUSED_COMBINE).
+ *                        256-byte aligned; contents on entry are ignored.
  * Asynchronous; CUDA-graph capturable (no allocation, no synchronisation). */
 fd_status fd_decode(const fd_desc* desc, const void* q, const void* k_cache,
                     const void* v_cache, const int32_t* seqlens, const int32_t* block_table,
@@ -244,17 +218,13 @@ fd_status fd_combine_states(const fd_desc* desc, const void* workspace, size_t w
                             void* out, float* lse, void* stream);
 
 /* Reads (and with clear != 0 resets) the current device's status word after
- * synchronising `stream`.  FD_OK, FD_ERR_DEVICE_TIMEOUT, FD_ERR_DEVICE_BOUNDS,
- * FD_ERR_WORKSPACE (a fused call found its ticket section not zeroed) or
- * FD_ERR_CUDA, in that order of precedence.  The word is sticky across calls
- * until cleared. */
+ * synchronising `stream`.  FD_OK, FD_ERR_DEVICE_TIMEOUT, FD_ERR_DEVICE_BOUNDS
+ * or FD_ERR_CUDA.  The word is sticky across calls until cleared. */
 fd_status fd_device_status(void* stream, int32_t clear);
 
 /* Size of the fixed device workspace behind fd_decode_static: 8 MiB, enough
- * for batch*q_len*n_q_heads*n_splits up to about 16000 query-row splits at
- * head_dim 128 (each needs (head_dim + 2) * 4 bytes, after the 64 KB ticket
- * section).  The array starts zeroed, so FD_FLAG_FUSED_COMBINE needs no
- * initialisation here. */
+ * for batch*n_q_heads*n_splits up to 16131 query-row splits at head_dim 128
+ * (each needs (head_dim + 2) * 4 bytes). */
 #define FD_STATIC_WORKSPACE_BYTES (8u << 20)
 
 /* fd_decode for callers that cannot allocate device memory.  The pages

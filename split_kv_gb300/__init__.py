@@ -38,17 +38,14 @@ FD_MAX_SPLITS = 128
 FD_TILE_TOKENS = 128
 FD_STATIC_WORKSPACE_BYTES = 8 << 20
 FD_FLAG_CUDA_CORES = 1
-FD_FLAG_FUSED_COMBINE = 1 << 1
 FD_FLAG_TEST_DROP_FIRST_STAGE = 1 << 16
-FD_TICKETS = 16384
-FD_TICKET_BYTES = 4 * FD_TICKETS
 
 LIB_PATH = _build.LIB_PATH
 
 # every function the header declares (checked against include/fd.h by the tests)
 EXPORTS = ("fd_abi_version", "fd_status_string", "fd_num_sms", "fd_plan_splits", "fd_plan",
            "fd_workspace_size", "fd_decode", "fd_split_states", "fd_combine_states",
-           "fd_device_status", "fd_decode_static", "fd_workspace_init")
+           "fd_device_status", "fd_decode_static")
 
 
 class FdDesc(ctypes.Structure):
@@ -113,7 +110,6 @@ def _load():
             "fd_combine_states": (i32, [dp, vp, sz, vp, vp, vp]),
             "fd_device_status": (i32, [vp, i32]),
             "fd_decode_static": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp]),
-            "fd_workspace_init": (i32, [vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -200,13 +196,6 @@ def fd_combine_states(desc: FdDesc, workspace, out, lse, workspace_bytes: int | 
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     return int(_load().fd_combine_states(ctypes.byref(desc), _ptr(workspace), int(wb), _ptr(out),
                                          _ptr(lse), _stream(stream)))
-
-
-def fd_workspace_init(workspace, workspace_bytes: int | None = None, stream=None) -> int:
-    """Zero the workspace's ticket section (needed once before its first call
-    with FD_FLAG_FUSED_COMBINE)."""
-    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
-    return int(_load().fd_workspace_init(_ptr(workspace), int(wb), _stream(stream)))
 
 
 def fd_decode_static(desc: FdDesc, q, k_cache, v_cache, seqlens, block_table, out, lse,

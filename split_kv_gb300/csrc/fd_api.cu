@@ -24,14 +24,10 @@ struct WsLayout {
     size_t off_u, off_m, off_l, total;
 };
 
-// Tickets of the fused combine first, at a fixed offset and size, so that a
-// zeroed ticket section stays valid whatever the shapes later calls use.
-constexpr size_t kTicketBytes = static_cast<size_t>(FD_TICKETS) * sizeof(uint32_t);
-
 WsLayout ws_layout(int64_t rows, int64_t splits) {
     WsLayout w;
-    w.off_u = kTicketBytes;
-    w.off_m = w.off_u + round_up(static_cast<size_t>(rows * splits * kHeadDim) * sizeof(float));
+    w.off_u = 0;
+    w.off_m = round_up(static_cast<size_t>(rows * splits * kHeadDim) * sizeof(float));
     w.off_l = w.off_m + round_up(static_cast<size_t>(rows * splits) * sizeof(float));
     w.total = w.off_l + round_up(static_cast<size_t>(rows * splits) * sizeof(float));
     return w;
@@ -63,7 +59,7 @@ int col_blocks_of(const fd_desc* d) {
 // done by the callers, which know which pointers they use.
 fd_status check_desc(const fd_desc* d) {
     if (d == nullptr) return FD_ERR_INVALID_ARG;
-    if ((d->flags & ~(FD_FLAG_CUDA_CORES | FD_FLAG_FUSED_COMBINE | FD_FLAG_TEST_DROP_FIRST_STAGE)) != 0)
+    if ((d->flags & ~(FD_FLAG_CUDA_CORES | FD_FLAG_TEST_DROP_FIRST_STAGE)) != 0)
         return FD_ERR_INVALID_ARG;
     if (d->q_len < 0) return FD_ERR_INVALID_ARG;
     if (d->batch < 0 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1)
@@ -168,16 +164,11 @@ fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
-// fused: the split kernel also merges (FD_FLAG_FUSED_COMBINE), writing out / lse.
 fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, const void* v,
                      const int32_t* seqlens, const int32_t* block_table, void* workspace,
-                     size_t workspace_bytes, cudaStream_t stream, bool fused = false,
-                     void* out = nullptr, float* lse = nullptr) {
+                     size_t workspace_bytes, cudaStream_t stream) {
     if (q == nullptr || k == nullptr || v == nullptr || seqlens == nullptr || workspace == nullptr)
         return FD_ERR_INVALID_ARG;
-    if (fused && (out == nullptr ||
-                  static_cast<int64_t>(d->batch) * d->n_kv_heads * col_blocks_of(d) > FD_TICKETS))
-        return out == nullptr ? FD_ERR_INVALID_ARG : FD_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FD_ERR_INVALID_ARG;
     const bool paged = d->page_size > 0;
     if (paged != (block_table != nullptr)) return FD_ERR_INVALID_ARG;
@@ -228,11 +219,6 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);
     p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
     p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
-    p.fused = fused ? 1 : 0;
-    p.out_dtype = d->out_dtype == FD_F16 ? 0 : d->out_dtype == FD_BF16 ? 1 : 2;
-    p.tickets = reinterpret_cast<unsigned*>(ws);
-    p.out = out;
-    p.lse = lse;
     const cudaError_t e = fdk::launch_split(tmK, tmV, p, q_type_of(d), is_fp8(d),
                                             (d->flags & FD_FLAG_CUDA_CORES) != 0, d->batch,
                                             d->n_kv_heads, stream);
@@ -345,10 +331,8 @@ fd_status fd_decode(const fd_desc* desc, const void* q, const void* k_cache, con
     const int32_t S = splits_for(desc);
     if (S < 1) return static_cast<fd_status>(S < 0 ? S : FD_ERR_INVALID_ARG);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool fused = (desc->flags & FD_FLAG_FUSED_COMBINE) != 0;
-    st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, workspace, workspace_bytes, s,
-                    fused, out, lse);
-    if (st != FD_OK || fused) return st;
+    st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, workspace, workspace_bytes, s);
+    if (st != FD_OK) return st;
     return combine_impl(desc, S, workspace, workspace_bytes, out, lse, s);
 }
 
@@ -366,20 +350,10 @@ fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cac
     st = static_workspace(&ws);
     if (st != FD_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool fused = (desc->flags & FD_FLAG_FUSED_COMBINE) != 0;
     st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, ws,
-                    FD_STATIC_WORKSPACE_BYTES, s, fused, out, lse);
-    if (st != FD_OK || fused) return st;
+                    FD_STATIC_WORKSPACE_BYTES, s);
+    if (st != FD_OK) return st;
     return combine_impl(desc, S, ws, FD_STATIC_WORKSPACE_BYTES, out, lse, s);
-}
-
-fd_status fd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
-        workspace_bytes < kTicketBytes)
-        return FD_ERR_WORKSPACE;
-    return cudaMemsetAsync(workspace, 0, kTicketBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? FD_OK
-               : FD_ERR_CUDA;
 }
 
 fd_status fd_device_status(void* stream, int32_t clear) {
@@ -387,9 +361,8 @@ fd_status fd_device_status(void* stream, int32_t clear) {
     if (fdk::read_status(&v, static_cast<cudaStream_t>(stream), clear != 0) != cudaSuccess)
         return FD_ERR_CUDA;
     if (v & fdk::kStatusTimeoutBit) return FD_ERR_DEVICE_TIMEOUT;
-    if (v & (fdk::kStatusSeqlenBit | fdk::kStatusPageBit)) return FD_ERR_DEVICE_BOUNDS;
-    if (v & fdk::kStatusTicketBit) return FD_ERR_WORKSPACE;
-    return v != 0 ? FD_ERR_DEVICE_BOUNDS : FD_OK;
+    if (v != 0) return FD_ERR_DEVICE_BOUNDS;
+    return FD_OK;
 }
 
 }  // extern "C"

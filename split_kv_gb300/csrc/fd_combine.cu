@@ -1,26 +1,41 @@
-// fd_combine.cu -- exact merge of the split states of each query row (the
-// rule and its citations are in fd_merge.cuh, shared with the fused tail of
-// the split kernel).
+// fd_combine.cu -- exact merge of the split states of each query row.
+//
+// For row r with states (u_i, m_i, l_i), i < n_splits:
+//   M = max over non-empty splits of m_i,   w_i = exp(m_i - M)   (0 if m_i = -inf)
+//   L = sum_i w_i l_i,   out = sum_i w_i u_i / L,   lse = M + log L
+// ("Decode 专项 Attention：把长KV拆开算，再正确合并" §04 and §06: an empty split
+// contributes zero and exp(-inf - (-inf)) is never evaluated; "Flash-Decoding:
+// Split-KV Attention for Long-Context Decode" §2, numerically stable form).
+// A row whose splits are all empty (sequence length 0) gets out = 0 and
+// lse = -inf.  The loop order over splits is fixed, so results are bitwise
+// repeatable from run to run.
 //
 // One CTA of 128 threads per row.  Launched with programmatic stream
 // serialization: it becomes resident while the split kernel runs and waits
 // (griddepcontrol.wait) for that kernel's states before reading them.
-#include "fd_merge.cuh"
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fd_device.cuh"
+#include "fd_internal.h"
 
 namespace fdk {
 
 namespace {
 
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;
+constexpr int kWarps = kHeadDim / 32;   // 4
 constexpr int kPre = 8;                 // splits per thread loaded up front (S <= 32: all)
 
-// Thread (w, lane) accumulates dims 4*lane..+3 over splits i = w, w+4, ...,
-// so the row's S x 128 partial outputs are all in flight at once (up to 32
-// splits together with m and l); the four warp partials are added in a
-// fixed order.
+// One CTA (4 warps) per row.  Thread (w, lane) accumulates dims 4*lane..+3
+// over splits i = w, w+4, ..., so the row's S x 128 partial outputs are all
+// in flight at once (up to 32 splits together with m and l); the four warp
+// partials are added in a fixed order.
 __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParams p) {
     __shared__ float s_m[kMaxSplits], s_w[kMaxSplits], s_l[kMaxSplits];
-    __shared__ float4 s_part[kMergeWarps][32];
+    __shared__ float4 s_part[kWarps][32];
     __shared__ float s_M, s_L;
     // let the next kernel in the stream get resident, then wait for the split
     // kernel (programmatic dependent launch) before reading its states
@@ -33,12 +48,11 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
     const int S = p.n_splits;
     // The partial outputs do not depend on m and l: request the first kPre of
     // this thread's splits now, so that they travel with m and l.
-    const float4* urow =
-        reinterpret_cast<const float4*>(p.ws_u + static_cast<int64_t>(row) * S * kHeadDim) + lane;
+    const float4* urow = reinterpret_cast<const float4*>(p.ws_u + static_cast<int64_t>(row) * S * kHeadDim) + lane;
     float4 pre[kPre];
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
-        const int i = w + kMergeWarps * k;
+        const int i = w + kWarps * k;
         pre[k] = i < S ? urow[i * (kHeadDim / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (t < S) {
@@ -46,21 +60,67 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
         s_l[t] = p.ws_l[static_cast<int64_t>(row) * S + t];
     }
     __syncthreads();
-    if (w == 0) merge_weights(s_m, s_l, S, s_w, &s_M, &s_L, lane);
+    if (w == 0) {
+        float M = -INFINITY;
+        for (int i = lane; i < S; i += 32) M = fmaxf(M, s_m[i]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+        float L = 0.f;
+        for (int i = lane; i < S; i += 32) {
+            const float m = s_m[i];
+            const float wt = (m == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2((m - M) * kLog2e);
+            s_w[i] = wt;
+            L = fmaf(wt, s_l[i], L);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
+        if (lane == 0) {
+            s_M = M;
+            s_L = L;
+        }
+    }
     __syncthreads();
 
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
-        const int i = w + kMergeWarps * k;
-        if (i < S) merge_step(a, s_w[i], pre[k]);
+        const int i = w + kWarps * k;
+        if (i < S) {
+            const float wt = s_w[i];
+            a.x = fmaf(wt, pre[k].x, a.x);
+            a.y = fmaf(wt, pre[k].y, a.y);
+            a.z = fmaf(wt, pre[k].z, a.z);
+            a.w = fmaf(wt, pre[k].w, a.w);
+        }
     }
 #pragma unroll 8
-    for (int i = w + kMergeWarps * kPre; i < S; i += kMergeWarps)
-        merge_step(a, s_w[i], urow[i * (kHeadDim / 4)]);
+    for (int i = w + kWarps * kPre; i < S; i += kWarps) {
+        const float wt = s_w[i];
+        const float4 u = urow[i * (kHeadDim / 4)];
+        a.x = fmaf(wt, u.x, a.x);
+        a.y = fmaf(wt, u.y, a.y);
+        a.z = fmaf(wt, u.z, a.z);
+        a.w = fmaf(wt, u.w, a.w);
+    }
     s_part[w][lane] = a;
     __syncthreads();
-    merge_store(s_part, s_M, s_L, t, row, p.out, p.out_dtype, p.lse);
+
+    const float M = s_M, L = s_L;
+    const bool empty = (M == -INFINITY) || !(L > 0.f);
+    // thread t writes dim t: component t % 4 of float4 t / 4
+    const int q4 = t >> 2, c = t & 3;
+    float u = 0.f;
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) u += reinterpret_cast<const float*>(&s_part[k][q4])[c];
+    const float o = empty ? 0.f : u / L;
+    const int64_t oi = static_cast<int64_t>(row) * kHeadDim + t;
+    if (p.out_dtype == 2)
+        static_cast<float*>(p.out)[oi] = o;
+    else if (p.out_dtype == 0)
+        static_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+    else
+        static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+    if (p.lse != nullptr && t == 0) p.lse[row] = empty ? -INFINITY : M + logf(L);
 }
 
 }  // namespace

@@ -29,7 +29,6 @@ inline int stage_tokens(bool fp8, int cols) { return fp8 && cols <= 8 ? kSubF8 :
 constexpr unsigned kStatusTimeoutBit = 1u;   // an mbarrier wait ran past its limit
 constexpr unsigned kStatusSeqlenBit = 2u;    // seqlens[b] < 0 or beyond the cache capacity
 constexpr unsigned kStatusPageBit = 4u;      // block-table entry outside [0, n_pages)
-constexpr unsigned kStatusTicketBit = 8u;    // a fused-combine ticket was not zero before the call
 
 struct SplitParams {
     const void* q;
@@ -54,14 +53,6 @@ struct SplitParams {
     float* ws_u;                    // [rows][n_splits][D]
     float* ws_m;                    // [rows][n_splits]
     float* ws_l;                    // [rows][n_splits]
-    // fused combine (fused != 0): the last CTA of each (b, KV head, column
-    // block) group, by the arrival ticket tickets[b * gridDim.y + blockIdx.y],
-    // merges the group's rows into out / lse and sets the ticket back to 0
-    int32_t fused;
-    int32_t out_dtype;              // 0 f16, 1 bf16, 2 f32
-    unsigned* tickets;
-    void* out;
-    float* lse;                     // or null
 };
 
 struct CombineParams {

@@ -36,7 +36,6 @@
 
 #include "fd_device.cuh"
 #include "fd_internal.h"
-#include "fd_merge.cuh"
 
 namespace fdk {
 
@@ -1041,77 +1040,6 @@ template <typename T> struct Consumer<T, 18> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 8>(c, w, l); }
 };
 
-// 16 bytes global -> shared through L2 only: the states were written by other
-// CTAs of this grid, and L1 is not coherent with their stores
-__device__ __forceinline__ void cp_async16_cg(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-                 "l"(gmem_src)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-// Fused combine, run by the last CTA of a (sequence, KV head, column block)
-// group once every split's states are written: merges the group's rows with
-// the combine kernel's arithmetic (fd_merge.cuh), so the two paths give the
-// same bits.  The rows' states are staged in the idle stage memory, as many
-// rows at a time as fit; per batch: weights (warp w takes rows w, w+4, ...),
-// then each warp's share of every row's weighted sum, then the outputs.
-// 128 threads (one per dim), named barrier 2.
-template <int KIND>
-__device__ void fused_merge(const SplitCtx& c, int S) {
-    using Gm = Geo<KIND>;
-    const SplitParams& p = *c.p;
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    const int ncols = min(kCols, p.cols - c.cb * kCols);
-    auto row_of = [&](int col) -> int64_t {
-        const int n = c.cb * kCols + col;
-        return (static_cast<int64_t>(c.b) * p.q_len + n / p.group) * p.n_q_heads +
-               c.kvh * p.group + n % p.group;
-    };
-    // per row: u [S][128] f32, warp partials [4][32] float4, m, l, w [S], M, L
-    const int row_bytes = S * (kHeadDim + 3) * 4 + kMergeWarps * 32 * 16 + 8;
-    const int nb_max = max(1, min(ncols, Gm::kOffBars / row_bytes));
-    for (int c0 = 0; c0 < ncols; c0 += nb_max) {
-        const int nb = min(nb_max, ncols - c0);
-        float* su = reinterpret_cast<float*>(c.smem);
-        float4* spart = reinterpret_cast<float4*>(su + nb * S * kHeadDim);
-        float* sm = reinterpret_cast<float*>(spart + nb * kMergeWarps * 32);
-        float* sl = sm + nb * S;
-        float* sw = sl + nb * S;
-        float* sM = sw + nb * S;
-        float* sL = sM + nb;
-        for (int idx = t; idx < nb * S * 32; idx += kHeadDim) {   // (row, split, 16-byte piece)
-            const int r = idx / (S * 32), rem = idx - r * S * 32;
-            cp_async16_cg(su + static_cast<int64_t>(r) * S * kHeadDim + rem * 4,
-                          p.ws_u + row_of(c0 + r) * S * kHeadDim + rem * 4);
-        }
-        for (int idx = t; idx < nb * S; idx += kHeadDim) {
-            const int r = idx / S, i = idx - r * S;
-            sm[idx] = __ldcg(p.ws_m + row_of(c0 + r) * S + i);
-            sl[idx] = __ldcg(p.ws_l + row_of(c0 + r) * S + i);
-        }
-        cp_async_wait_all();
-        named_sync(2, kHeadDim);
-        for (int r = w; r < nb; r += kMergeWarps)
-            merge_weights(sm + r * S, sl + r * S, S, sw + r * S, sM + r, sL + r, lane);
-        named_sync(2, kHeadDim);
-        for (int r = 0; r < nb; ++r) {
-            const float4* ur = reinterpret_cast<const float4*>(su + static_cast<int64_t>(r) * S * kHeadDim) + lane;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int i = w; i < S; i += kMergeWarps) merge_step(a, sw[r * S + i], ur[i * (kHeadDim / 4)]);
-            spart[(r * kMergeWarps + w) * 32 + lane] = a;
-        }
-        named_sync(2, kHeadDim);
-        for (int r = 0; r < nb; ++r)
-            merge_store(reinterpret_cast<const float4(*)[32]>(spart + r * kMergeWarps * 32), sM[r], sL[r],
-                        t, row_of(c0 + r), p.out, p.out_dtype, p.lse);
-        named_sync(2, kHeadDim);   // the scratch is restaged for the next batch
-    }
-}
-
 template <typename T, int KIND>
 __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -1182,9 +1110,8 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
         return;
     }
 
-    // false after a timeout (uniform over the consumer warps): no states then
-    const bool ok = Consumer<T, KIND>::run(c, warp, lane);
-    if (ok) named_sync(1, kWarps * 32);
+    if (!Consumer<T, KIND>::run(c, warp, lane)) return;
+    named_sync(1, kWarps * 32);
     if (threadIdx.x >= kHeadDim) return;   // one thread per dim below
 
     // ---- merge the consumer warps' states of each column and write the split's state
@@ -1192,7 +1119,7 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     const float* wm = reinterpret_cast<const float*>(smem + Gm::kOffWM);
     const float* wl = reinterpret_cast<const float*>(smem + Gm::kOffWL);
     const int d = threadIdx.x;   // 0 .. 127
-    const int ncols = ok ? min(kCols, p.cols - c.cb * kCols) : 0;
+    const int ncols = min(kCols, p.cols - c.cb * kCols);
     for (int col = 0; col < ncols; ++col) {
         float M = -INFINITY;
 #pragma unroll
@@ -1219,27 +1146,6 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
             p.ws_l[idx] = l;
         }
     }
-    if (!p.fused) return;
-
-    // ---- fused combine: every CTA of the group takes an arrival ticket after
-    // its states are visible; the one that takes ticket S - 1 merges the
-    // group's rows and sets the ticket back to 0.  A CTA that timed out still
-    // takes its ticket, so the ticket returns to 0 (the status word has the
-    // timeout).  A ticket found at S or above means it was not 0 before the call.
-    __threadfence();
-    named_sync(2, kHeadDim);
-    volatile int* s_last = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 8);
-    unsigned* ticket = p.tickets + static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y;
-    if (threadIdx.x == 0) {
-        const unsigned tk = atomicAdd(ticket, 1u);
-        if (tk >= static_cast<unsigned>(S)) raise_status(kStatusTicketBit);
-        *s_last = tk == static_cast<unsigned>(S - 1) ? 1 : 0;
-    }
-    named_sync(2, kHeadDim);
-    if (*s_last == 0) return;
-    __threadfence();   // the other CTAs' states, before reading them
-    fused_merge<KIND>(c, S);
-    if (threadIdx.x == 0) *ticket = 0u;
 }
 
 template <typename T, int KIND>

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(fd):
 
 
 def test_abi_version_and_strings(fd):
-    assert fd.fd_abi_version() == 4
+    assert fd.fd_abi_version() == 3
     for code in range(-6, 1):
         s = fd.fd_status_string(code)
         assert s and s != "unknown status"
@@ -122,7 +122,7 @@ def test_workspace_size_layout(fd):
     rows, S, D = 32, 4, 128
     def r256(x):
         return (x + 255) // 256 * 256
-    want = fd.FD_TICKET_BYTES + r256(rows * S * D * 4) + 2 * r256(rows * S * 4)
+    want = r256(rows * S * D * 4) + 2 * r256(rows * S * 4)
     assert fd.fd_workspace_size(d, 4) == want
     assert fd.fd_workspace_size(d, 129) == 0
     assert fd.fd_workspace_size(_desc(fd, head_dim=64), 4) == 0
@@ -158,17 +158,7 @@ def test_decode_rejects_bad_arguments_without_a_gpu(fd):
     assert call(_desc(fd, out_dtype=9)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, n_splits=129)) == fd.FD_ERR_UNSUPPORTED
     assert call(_desc(fd, k_stride_t=100)) == fd.FD_ERR_INVALID_ARG          # not 16-byte multiple
-    assert call(_desc(fd, flags=4)) == fd.FD_ERR_INVALID_ARG               # an undefined flag bit
-    fu = fd.FD_FLAG_FUSED_COMBINE
-    assert call(_desc(fd, flags=fu), out=None) == fd.FD_ERR_INVALID_ARG
-    # more (sequence, KV head) groups than tickets
-    many = dict(batch=fd.FD_TICKETS + 1, n_q_heads=4, n_kv_heads=1, q_stride_b=4 * 128,
-                k_stride_b=1024 * 128, k_stride_h=1024 * 128, v_stride_b=1024 * 128,
-                v_stride_h=1024 * 128, n_splits=2)
-    assert call(_desc(fd, flags=fu, **many)) == fd.FD_ERR_UNSUPPORTED
-    assert fd.fd_workspace_init(None, big, stream=0) == fd.FD_ERR_WORKSPACE
-    assert fd.fd_workspace_init(ws + 64, big, stream=0) == fd.FD_ERR_WORKSPACE
-    assert fd.fd_workspace_init(ws, fd.FD_TICKET_BYTES - 4, stream=0) == fd.FD_ERR_WORKSPACE
+    assert call(_desc(fd, flags=2)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, kv_extent=0)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, page_size=12, max_pages_per_seq=4)) == fd.FD_ERR_INVALID_ARG
     assert call(_desc(fd, page_size=4, max_pages_per_seq=4), bt=fake) == fd.FD_ERR_UNSUPPORTED

@@ -230,13 +230,12 @@ def _states_workspace(desc, S, m, l, u):
     rows = desc.batch * desc.n_q_heads
     D = desc.head_dim
     r256 = lambda x: (x + 255) // 256 * 256
-    off_u = fd.FD_TICKET_BYTES                  # after the fused-combine tickets
-    off_m = off_u + r256(rows * S * D * 4)
+    off_m = r256(rows * S * D * 4)
     off_l = off_m + r256(rows * S * 4)
     wsb = fd.fd_workspace_size(desc, S)
-    assert wsb == off_l + r256(rows * S * 4)
+    assert wsb >= off_l + rows * S * 4
     ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
-    ws[off_u:off_u + rows * S * D * 4].view(torch.float32).copy_(torch.tensor(u, dtype=torch.float32).reshape(-1))
+    ws[:rows * S * D * 4].view(torch.float32).copy_(torch.tensor(u, dtype=torch.float32).reshape(-1))
     ws[off_m:off_m + rows * S * 4].view(torch.float32).copy_(torch.tensor(m, dtype=torch.float32).reshape(-1))
     ws[off_l:off_l + rows * S * 4].view(torch.float32).copy_(torch.tensor(l, dtype=torch.float32).reshape(-1))
     return ws, wsb
