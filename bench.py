@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -169,11 +170,19 @@ def _traffic_from_profile(src_hash: str):
     return None
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed, so that
+    a comment-only edit keeps a profile's counters attached to the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
 def _kernel_hash():
     h = hashlib.sha256()
     for name in ("fd_split.cu", "fd_device.cuh", "fd_internal.h"):
-        with open(os.path.join(ROOT, "split_kv_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "split_kv_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 
