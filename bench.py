@@ -345,25 +345,48 @@ def run_gpu(args):
     value = job_bytes / (ms * 1e-3) / 1e9
     us_layer = ms * 1e3 / n_layers
 
-    # ---- roofline of fd_split: per-launch CUDA events around the kernel alone
+    # ---- roofline of fd_split.  The kernel's time per launch: its n_layers
+    # launches back to back, captured in a CUDA graph and replayed between
+    # CUDA events on the replay stream (as in the timed step, but without the
+    # combine); the combine likewise.  Per-launch events around eager
+    # launches, which include each launch's gap, are reported beside it.
+    reps = max(3, min(20, args.steps // 10))
+
+    def splits(h):
+        for i in range(n_layers):
+            fd.check(fd.fd_split_states(desc, qs[i], ks[i], vs[i], seqlens, None, workspace, wsb, stream=h))
+
+    def combines(h):
+        for i in range(n_layers):
+            fd.check(fd.fd_combine_states(desc, workspace, out[i], lse[i], wsb, stream=h))
+
+    def per_launch_ms(body):
+        g, _ = _capture(body, dev, stream, args.eager)
+        run = g.replay if g is not None else (lambda: body(sp))
+        run()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            run()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / (reps * n_layers)
+
+    split_avg_ms = per_launch_ms(splits)
+    combine_avg_ms = per_launch_ms(combines)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_layers)]
-    split_ms, combine_ms = [], []
-    ec = [torch.cuda.Event(enable_timing=True) for _ in range(n_layers)]
-    for rep in range(max(3, min(20, args.steps // 10))):
+    split_eager_ms = []
+    for rep in range(reps):
         for i in range(n_layers):
             ev[i][0].record(stream)
             fd.check(fd.fd_split_states(desc, qs[i], ks[i], vs[i], seqlens, None, workspace, wsb, stream=sp))
             ev[i][1].record(stream)
             fd.check(fd.fd_combine_states(desc, workspace, out[i], lse[i], wsb, stream=sp))
-            ec[i].record(stream)
         torch.cuda.synchronize()
-        if rep == 0:
-            continue   # warm-up pass
-        for i in range(n_layers):
-            split_ms.append(ev[i][0].elapsed_time(ev[i][1]))
-            combine_ms.append(ev[i][1].elapsed_time(ec[i]))
-    split_avg_ms = statistics.mean(split_ms)
+        if rep > 0:   # the first pass warms up
+            split_eager_ms += [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_layers)]
     ws_write = B * Hq * S * (D + 2) * 4
     split_alg_bytes = kv_bytes_layer + B * Hq * D * 2 + ws_write + 4 * B
     peak, peak_src = _peaks()
@@ -372,7 +395,10 @@ def run_gpu(args):
     roofline = {"kernel": "fd_split", "bound": "hbm", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": peak_src, "alg_bytes_per_launch": split_alg_bytes,
-                "launch_us": split_avg_ms * 1e3, "combine_us": statistics.mean(combine_ms) * 1e3}
+                "launch_us": split_avg_ms * 1e3,
+                "launch_timing": f"{n_layers} back-to-back launches per replay, {reps} replays",
+                "launch_us_eager_events": statistics.mean(split_eager_ms) * 1e3,
+                "combine_us": combine_avg_ms * 1e3}
 
     # ---- e2e: public API from pinned host buffers, one layer per step
     e2e = None
