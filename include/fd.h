@@ -183,6 +183,9 @@ int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t he
 size_t fd_workspace_size(const fd_desc* desc, int32_t n_splits);
 
 /* The whole decode step: fd_split_states then fd_combine_states on `stream`.
+ * With one split (n_splits = 1, given or planned) a row's state is already
+ * its result: the split kernel writes out and lse itself (the combine's
+ * arithmetic at one split, so the same bits) and the workspace is not used.
  *  q, k_cache, v_cache : device, layouts in fd_desc.
  *  seqlens             : device int32[batch], 0 <= seqlens[b] <= capacity,
  *                        capacity = kv_extent (contiguous) or

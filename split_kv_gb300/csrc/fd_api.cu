@@ -164,9 +164,11 @@ fd_status make_map(CUtensorMap* map, const fd_desc* d, const void* base, int64_t
     return r == CUDA_SUCCESS ? FD_OK : FD_ERR_INVALID_ARG;
 }
 
+// direct (S = 1 only): the split kernel writes out / lse itself, no combine.
 fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, const void* v,
                      const int32_t* seqlens, const int32_t* block_table, void* workspace,
-                     size_t workspace_bytes, cudaStream_t stream) {
+                     size_t workspace_bytes, cudaStream_t stream, bool direct = false,
+                     void* out = nullptr, float* lse = nullptr) {
     if (q == nullptr || k == nullptr || v == nullptr || seqlens == nullptr || workspace == nullptr)
         return FD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FD_ERR_INVALID_ARG;
@@ -219,6 +221,10 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.ws_u = reinterpret_cast<float*>(ws + w.off_u);
     p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
     p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
+    p.direct = direct && S == 1 && out != nullptr ? 1 : 0;
+    p.out_dtype = d->out_dtype == FD_F16 ? 0 : d->out_dtype == FD_BF16 ? 1 : 2;
+    p.out = out;
+    p.lse = lse;
     const cudaError_t e = fdk::launch_split(tmK, tmV, p, q_type_of(d), is_fp8(d),
                                             (d->flags & FD_FLAG_CUDA_CORES) != 0, d->batch,
                                             d->n_kv_heads, stream);
@@ -331,8 +337,10 @@ fd_status fd_decode(const fd_desc* desc, const void* q, const void* k_cache, con
     const int32_t S = splits_for(desc);
     if (S < 1) return static_cast<fd_status>(S < 0 ? S : FD_ERR_INVALID_ARG);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, workspace, workspace_bytes, s);
-    if (st != FD_OK) return st;
+    // one split: the split kernel writes the result itself (no combine launch)
+    st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, workspace, workspace_bytes, s,
+                    S == 1, out, lse);
+    if (st != FD_OK || S == 1) return st;
     return combine_impl(desc, S, workspace, workspace_bytes, out, lse, s);
 }
 
@@ -351,8 +359,8 @@ fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cac
     if (st != FD_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, ws,
-                    FD_STATIC_WORKSPACE_BYTES, s);
-    if (st != FD_OK) return st;
+                    FD_STATIC_WORKSPACE_BYTES, s, S == 1, out, lse);
+    if (st != FD_OK || S == 1) return st;
     return combine_impl(desc, S, ws, FD_STATIC_WORKSPACE_BYTES, out, lse, s);
 }
 

@@ -53,6 +53,12 @@ struct SplitParams {
     float* ws_u;                    // [rows][n_splits][D]
     float* ws_m;                    // [rows][n_splits]
     float* ws_l;                    // [rows][n_splits]
+    // direct != 0 (one split): each row's state is its result, so the kernel
+    // writes out = u / l and lse = m + log l itself instead of the state
+    int32_t direct;
+    int32_t out_dtype;              // 0 f16, 1 bf16, 2 f32
+    void* out;                      // [rows][D]
+    float* lse;                     // [rows] or null
 };
 
 struct CombineParams {

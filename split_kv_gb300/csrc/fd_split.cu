@@ -1140,7 +1140,24 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
         const int64_t row = (static_cast<int64_t>(c.b) * p.q_len + i) * p.n_q_heads +
                             c.kvh * p.group + g;
         const int64_t idx = row * S + c.split;
-        p.ws_u[idx * kHeadDim + d] = u * p.v_scale;   // values are v_scale x the stored ones
+        const float us = u * p.v_scale;   // values are v_scale x the stored ones
+        if (p.direct) {
+            // One split: the merge of a single state (weight exp(0) = 1) is
+            // out = u / l, lse = m + log l; the same operations here give the
+            // combine kernel's bits without its launch.
+            const bool empty = m_out == -INFINITY || !(l > 0.f);
+            const float o = empty ? 0.f : us / l;
+            const int64_t oi = row * kHeadDim + d;
+            if (p.out_dtype == 2)
+                static_cast<float*>(p.out)[oi] = o;
+            else if (p.out_dtype == 0)
+                static_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+            else
+                static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+            if (d == 0 && p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l);
+            continue;
+        }
+        p.ws_u[idx * kHeadDim + d] = us;
         if (d == 0) {
             p.ws_m[idx] = m_out;
             p.ws_l[idx] = l;

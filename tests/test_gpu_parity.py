@@ -225,6 +225,60 @@ def test_bitwise_repeatable_and_halves_equal_whole():
     assert np.array_equal(lse.cpu().double().numpy().reshape(-1), l1)
 
 
+@pytest.mark.parametrize("kind", ["f16", "bf16_cuda_cores", "fp8_block"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_one_split_writes_the_result_directly(kind, out_dtype):
+    """With one split fd_decode (and fd_decode_static) skip the combine: the
+    split kernel writes out / lse itself.  The bits must be those of
+    fd_split_states + fd_combine_states, including an empty row, and the
+    workspace must be left untouched."""
+    B, Hkv, D, T = 3, 2, 128, 1500
+    lens = np.array([1500, 77, 0], dtype=np.int32)
+    flags, sc = 0, {}
+    if kind == "fp8_block":
+        if not hasattr(torch, "float8_e4m3fn"):
+            pytest.skip("torch without float8_e4m3fn")
+        G, ql = 4, 3
+        k = fd_inputs.randn_fp8((B, Hkv, T, D), 1951, device=DEV, gain=16.0)
+        v = fd_inputs.randn_fp8((B, Hkv, T, D), 1952, device=DEV, gain=16.0)
+        q = fd_inputs.randn((B, ql, Hkv * G, D), "bf16", 1953, device=DEV)
+        sc = dict(k_scale=1 / 16, v_scale=1 / 16)
+    else:
+        G, ql = 4, 1
+        dt = "f16" if kind == "f16" else "bf16"
+        k, v = _cache(B, Hkv, T, D, dt, 1954)
+        q = fd_inputs.randn((B, Hkv * G, D), dt, 1955, device=DEV)
+        flags = fd.FD_FLAG_CUDA_CORES if "cuda_cores" in kind else 0
+    Hq = Hkv * G
+    seqlens = torch.from_numpy(lens).to(DEV)
+    desc = fd.make_desc(q, k, v, max_seqlen=int(lens.max()), n_splits=1, out_dtype=out_dtype, **sc)
+    desc.flags = flags
+    wsb = fd.fd_workspace_size(desc, 1)
+    shape = (B, ql, Hq, D)
+    results = []
+    for mode in ("two_kernels", "decode", "static"):
+        ws = torch.full((wsb,), 0x5A, dtype=torch.uint8, device=DEV)
+        out = torch.full(shape, float("nan"), dtype=out_dtype, device=DEV)
+        lse = torch.full((B, ql, Hq), float("nan"), dtype=torch.float32, device=DEV)
+        if mode == "two_kernels":
+            fd.check(fd.fd_split_states(desc, q, k, v, seqlens, None, ws))
+            fd.check(fd.fd_combine_states(desc, ws, out, lse))
+        elif mode == "decode":
+            fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, lse, ws))
+        else:
+            fd.check(fd.fd_decode_static(desc, q, k, v, seqlens, None, out, lse))
+        torch.cuda.synchronize()
+        if mode == "decode":   # the direct path does not touch the workspace
+            assert bool((ws == 0x5A).all())
+        results.append((out.view(torch.int16 if out_dtype != torch.float32 else torch.int32).clone(),
+                        lse.view(torch.int32).clone()))
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    for o, l in results[1:]:
+        assert torch.equal(o, results[0][0]) and torch.equal(l, results[0][1])
+    lse0 = results[0][1].view(torch.float32).cpu().numpy().reshape(B, ql * Hq)
+    assert np.all(np.isneginf(lse0[2]))          # the empty row
+
+
 def _states_workspace(desc, S, m, l, u):
     """A workspace in the documented layout filled with caller states."""
     rows = desc.batch * desc.n_q_heads
