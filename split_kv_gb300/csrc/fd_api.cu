@@ -179,7 +179,7 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FD_ERR_WORKSPACE;
     if (workspace_bytes < w.total) return FD_ERR_WORKSPACE;
     if (d->batch == 0) return FD_OK;
-    if (d->batch > 65535 || static_cast<int64_t>(d->n_kv_heads) * col_blocks_of(d) > 65535)
+    if (d->batch > 65535 || d->n_kv_heads > 65535)   // grid (S * col_blocks, n_kv_heads, batch)
         return FD_ERR_UNSUPPORTED;
 
     CUtensorMap tmK, tmV;

@@ -208,7 +208,9 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
     constexpr int kStageBytes = Gm::kStageBytes;
     constexpr int kSub = Gm::kSub;
     const SplitParams& p = *c.p;
-    const uint64_t policy = policy_evict_first();
+    // K/V are read once (evict first), or once per column block of the split
+    // (kept at normal priority for the sibling CTAs that read them next)
+    const uint64_t policy = p.col_blocks > 1 ? policy_evict_normal() : policy_evict_first();
     const bool paged = p.page_size != 0;
     const int rows = paged ? min(kPagedBoxRows, p.page_size) : kSub;   // tokens per box
     const int nbox = kSub / rows;                                        // boxes per half per stage
@@ -1055,9 +1057,12 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     c.stages = kRing;
     c.p = &p;
     c.smem = smem;
-    c.split = blockIdx.x;
-    c.kvh = blockIdx.y / p.col_blocks;
-    c.cb = blockIdx.y % p.col_blocks;
+    // grid (n_splits * col_blocks, n_kv_heads, batch): the column blocks of
+    // one split are adjacent, so they run together and the later readers of
+    // the split's K/V find it in L2
+    c.split = blockIdx.x / p.col_blocks;
+    c.cb = blockIdx.x % p.col_blocks;
+    c.kvh = blockIdx.y;
     c.b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1091,7 +1096,7 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     // a page and a paged cache splits exactly like a contiguous one
     int L = __ldg(p.seqlens + c.b);
     if (L < 0 || L > p.capacity) {
-        if (threadIdx.x == 0 && c.split == 0 && blockIdx.y == 0) raise_status(kStatusSeqlenBit);
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_status(kStatusSeqlenBit);
         L = L < 0 ? 0 : p.capacity;
     }
     c.L = L;
@@ -1181,7 +1186,7 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    return launch_pdl(kern, dim3(p.n_splits, n_kv_heads * p.col_blocks, batch),
+    return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
                       dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
