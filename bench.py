@@ -59,7 +59,7 @@ def _args():
                     help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
     ap.add_argument("--workload", default=None,
                     choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep",
-                             "query_block_q4", "long_gqa_128k_fp8"],
+                             "query_block_q4", "long_gqa_128k_fp8", "sweep_fp8"],
                     help="time one workload (one JSON line per problem) instead of the default line")
     return ap.parse_args()
 
@@ -629,7 +629,8 @@ def run_suite(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     name = args.workload
     c = fd_inputs.WORKLOADS[name]
-    if name == "sweep":
+    grid = "batches" in c   # a sweep over batch x context
+    if grid:
         probs = [(b, t) for b in c["batches"] for t in c["ctxs"]]
         base = dict(c, batch=None, ctx=None, dtype=c["dtype"])
     else:
@@ -654,7 +655,7 @@ def run_suite(args):
             assert S_plan == fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
         results = {}
         for label, S in (("planned", S_plan), ("unsplit", 1)):
-            if label == "unsplit" and (name != "sweep" or S_plan == 1):
+            if label == "unsplit" and (not grid or S_plan == 1):
                 continue   # with a one-split plan the two are the same launch
             descs = []
             for (desc, q, k, v, bt) in sets:
@@ -686,7 +687,7 @@ def run_suite(args):
                 "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
                 "input_sets": n_sets, "kv_bytes": kv_bytes, "launch": note,
                 "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores"}
-        if name == "sweep":
+        if grid:
             S1, ms1 = results.get("unsplit", results["planned"])
             line["us_per_call_unsplit"] = ms1 * 1e3
             line["kv_gbs_unsplit"] = kv_bytes / (ms1 * 1e-3) / 1e9

@@ -21,6 +21,7 @@ Workloads (the pages measure on no dataset; every input is synthetic):
                  positions per sequence (a speculative-verification block).
   long_gqa_128k_fp8  the headline shape with an E4M3 cache (q fp16), values
                  stored x64 with k_scale = v_scale = 1/64.
+  sweep_fp8     the sweep's grid over such an E4M3 cache.
 K, V and q are i.i.d. N(0,1) cast to the cache dtype.
 """
 from __future__ import annotations
@@ -40,6 +41,10 @@ WORKLOADS = {
                      dtype="bf16", seed=1004, page_size=16),
     "sweep": dict(batches=(1, 4, 16, 64), ctxs=(1024, 8192, 32768, 131072, 262144),
                   n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="f16", seed=1005),
+    # the same grid over an E4M3 cache (q fp16), values stored x64, scales 1/64
+    "sweep_fp8": dict(batches=(1, 4, 16, 64), ctxs=(1024, 8192, 32768, 131072, 262144),
+                      n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="f16", kv_dtype="e4m3",
+                      kv_gain=64.0, seed=1008),
     # the headline shape with an fp8 (E4M3) cache, one scale per tensor:
     # stored = value * kv_gain, k_scale = v_scale = 1 / kv_gain
     "long_gqa_128k_fp8": dict(batch=1, n_q_heads=32, n_kv_heads=8, head_dim=128, ctx=128000,
