@@ -129,6 +129,23 @@ def test_workspace_size_layout(fd):
     assert fd.fd_workspace_size(_desc(fd, n_kv_heads=5), 4) == 0
 
 
+def test_workspace_size_for_query_blocks_and_fp8(fd):
+    """rows = batch * q_len * n_q_heads for a query block; an fp8 cache
+    changes nothing in the workspace (states are fp32 either way)."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for B, Hq, ql, S in ((1, 32, 4, 9), (3, 64, 8, 7), (2, 16, 16, 1)):
+        d = _desc(fd, batch=B, n_q_heads=Hq, q_len=ql, q_stride_t=Hq * 128, q_stride_b=ql * Hq * 128)
+        rows = B * ql * Hq
+        want = r256(rows * S * 128 * 4) + 2 * r256(rows * S * 4)
+        assert fd.fd_workspace_size(d, S) == want, (B, Hq, ql, S)
+        d8 = _desc(fd, batch=B, n_q_heads=Hq, q_len=ql, q_stride_t=Hq * 128, q_stride_b=ql * Hq * 128,
+                   kv_dtype=fd.FD_E4M3, q_dtype=fd.FD_BF16, k_scale=0.25, v_scale=4.0)
+        assert fd.fd_workspace_size(d8, S) == want
+    # a query block wider than the supported limits is invalid, so its size is 0
+    assert fd.fd_workspace_size(_desc(fd, q_len=17, q_stride_t=32 * 128), 4) == 0
+
+
 def test_decode_rejects_bad_arguments_without_a_gpu(fd):
     """Every rejection happens on the host, before any CUDA call."""
     fake = 1 << 20        # a 16-byte-aligned address that is never dereferenced
