@@ -648,8 +648,9 @@ def run_suite(args):
         kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * esize * 2
         ql = c.get("q_len", 1)
         cols = (c["n_q_heads"] // c["n_kv_heads"]) * ql
-        cblocks = 1 if cols <= 8 else -(-cols // 16)     # CTAs per split (query blocks)
-        S_plan = fd.fd_plan_splits(B * c["n_kv_heads"] * cblocks, 2 * fd.fd_num_sms(),
+        umma = c.get("kv_dtype") != "e4m3" and not args.cuda_cores and 16 < cols <= 128
+        cblocks = 1 if (umma or cols <= 8) else -(-cols // 16)     # CTAs per split (query blocks)
+        S_plan = fd.fd_plan_splits(B * c["n_kv_heads"] * cblocks, (1 if umma else 2) * fd.fd_num_sms(),
                                    -(-int(sl_h.max()) // 128))
         if ql == 1:
             assert S_plan == fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)

@@ -42,9 +42,11 @@
  *    first seqlens[b] - q_len + 1 + i keys (the block's own tokens are
  *    already in the cache, in order); a position that sees no key gets
  *    out = 0 and lse = -inf.  Every (position, head) of a KV head's group is
- *    one column of the CTA's tensor-core tile: up to 16 columns per CTA; a
- *    group with more columns uses ceil(G*q_len/16) CTAs per split, each
- *    reading the split's K/V once.
+ *    one column of the CTA's tensor-core tile.  Up to 16 columns: one CTA per
+ *    split on warp MMAs.  17-128 columns with a 16-bit cache (and no
+ *    FD_FLAG_CUDA_CORES): one CTA per split on tcgen05 MMAs, all columns as
+ *    the M rows of one 128-row tile.  Otherwise ceil(G*q_len/16) CTAs per
+ *    split, each reading the split's K/V once.
  *  - Supported shapes: head_dim 128; G = n_q_heads / n_kv_heads and q_len
  *    with G*q_len <= 256 and q_len <= 16 (with FD_FLAG_CUDA_CORES: G in
  *    {1, 2, 4, 8}, q_len = 1 and a 16-bit cache); kv_dtype FD_F16, FD_BF16 or
@@ -167,7 +169,9 @@ int32_t fd_plan_splits(int64_t work_items, int64_t slots, int64_t n_kv_blocks,
  * depends only on batch, n_kv_heads, max seqlen and num_sms; n_q_heads and
  * head_dim are validated only.  Returns s in [1, 128] or a negative fd_status.
  * (fd_decode, given n_splits <= 0, plans query blocks the same way with
- * work = batch*n_kv_heads*ceil(G*q_len/16), the CTAs per split.) */
+ * work = the CTAs per split: batch*n_kv_heads for up to 16 columns, and for
+ * the tcgen05 tile of 17-128 columns (16-bit cache), whose CTA fills an SM,
+ * with slots = num_sms; batch*n_kv_heads*ceil(G*q_len/16) otherwise.) */
 int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                 const int32_t* seqlens_host, int32_t num_sms);
 

@@ -51,9 +51,13 @@ int64_t rows_of(const fd_desc* d) {
     return static_cast<int64_t>(d->batch) * q_len_of(d) * d->n_q_heads;
 }
 
-int col_blocks_of(const fd_desc* d) {
-    return fdk::column_blocks((d->n_q_heads / d->n_kv_heads) * q_len_of(d));
+int cols_of(const fd_desc* d) { return (d->n_q_heads / d->n_kv_heads) * q_len_of(d); }
+
+bool umma_of(const fd_desc* d) {
+    return fdk::use_umma(is_fp8(d), (d->flags & FD_FLAG_CUDA_CORES) != 0, cols_of(d));
 }
+
+int col_blocks_of(const fd_desc* d) { return umma_of(d) ? 1 : fdk::column_blocks(cols_of(d)); }
 
 // Shape / layout checks shared by every entry point.  Pointer checks are
 // done by the callers, which know which pointers they use.
@@ -110,8 +114,9 @@ int32_t splits_for(const fd_desc* d) {
     const int32_t sms = fd_num_sms(-1);
     if (sms < 0) return sms;
     const int64_t blocks = (static_cast<int64_t>(d->max_seqlen) + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS;
+    // two CTAs per SM, or one for the tcgen05 variant
     return fd_plan_splits(static_cast<int64_t>(d->batch) * d->n_kv_heads * col_blocks_of(d),
-                          2 * static_cast<int64_t>(sms), blocks, FD_MAX_SPLITS);
+                          (umma_of(d) ? 1 : 2) * static_cast<int64_t>(sms), blocks, FD_MAX_SPLITS);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

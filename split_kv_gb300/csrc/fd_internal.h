@@ -102,6 +102,14 @@ cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const S
 
 // CTAs per (split, KV head) for G * q_len columns.
 inline int column_blocks(int cols) { return cols <= 8 ? 1 : (cols + 15) / 16; }
+
+// Query blocks wider than 16 columns (16-bit caches, tensor-core path) run
+// the tcgen05 variant: one CTA serves all columns (up to 128) and takes a
+// whole SM, so it is one work item per split and the planner counts one
+// slot per SM.
+inline bool use_umma(bool fp8, bool cuda_cores, int cols) {
+    return !fp8 && !cuda_cores && cols > 16 && cols <= 128;
+}
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Device status word helpers (fd_split.cu owns the symbol).

@@ -158,23 +158,30 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 // holds 96 KB, and two CTAs fit on an SM.
 template <int KIND>
 struct Geo {
-    static constexpr bool kF8 = KIND >= 20;
-    static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kConsumerWarps;
-    static constexpr int kSub = 16 * kWarps;                   // tokens per stage
-    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kStages;
+    static constexpr bool kUmma = KIND == 31;                  // tcgen05 consumer, see below
+    static constexpr bool kF8 = KIND >= 20 && !kUmma;
+    static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kUmma ? 8 : kConsumerWarps;
+    static constexpr int kSub = kUmma ? 64 : 16 * kWarps;      // tokens per stage
+    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kUmma ? 4 : kStages;
     static constexpr int kTile = kSub * 128;                   // one box of 128-byte rows
     static constexpr int kStageBytes = (kF8 ? 2 : 4) * kTile;
-    static constexpr int kOffBars = kRing * kStageBytes;       // full[kRing], empty[kRing]
-    static constexpr int kOffFlag = (kF8 ? kOffBars + 128 : fdk::kOffFlag);
-    static constexpr int kSmem = (kF8 ? kOffFlag + 16 : kSmemUsed) + 1024;   // + alignment slack
-    static constexpr int kThreads = (kWarps + 1) * 32;         // + one TMA producer warp
+    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile, P hi, P lo
+    static constexpr int kExtraBytes = kUmma ? 2 * 16384 + 2 * 16384 + 4096 : 0;   // + softmax pair exchange
+    static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing] (+ tcgen05 barriers)
+    static constexpr bool kOwnMap = kF8 || kUmma;
+    static_assert(!kUmma || kSub == fdk::kSub, "the tcgen05 variant streams the 16-bit stages");
+    static constexpr int kOffFlag = (kOwnMap ? kOffBars + 128 : fdk::kOffFlag);
+    static constexpr int kSmem = (kOwnMap ? kOffFlag + 16 : kSmemUsed) + 1024;   // + alignment slack
+    // + one TMA producer warp (+ one MMA-issuing warp for tcgen05)
+    static constexpr int kThreads = (kWarps + (kUmma ? 2 : 1)) * 32;
+    static constexpr int kEmptyArrivals = kUmma ? 1 : kWarps;  // tcgen05: the MMA commit
     // end-of-split merge area in stage memory: acc [warps][16][128], m, l [warps][16]
     static constexpr int kOffWM = kWarps * kCols * kHeadDim * 4;
     static constexpr int kOffWL = kOffWM + kWarps * kCols * 4;
-    static_assert(2 * kRing * 8 <= 128, "barriers must fit");
+    static_assert(2 * kRing * 8 + (kUmma ? 6 * 8 + 8 : 0) <= 128, "barriers must fit");
     static_assert(kOffWL + kWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
-    static_assert(kF8 || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
-                          kOffBars == fdk::kOffBars), "16-bit variants use the map above");
+    static_assert(kOwnMap || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
+                              kOffBars == fdk::kOffBars), "16-bit variants use the map above");
 };
 
 // Everything a CTA knows about its split, shared by the producer and consumers.
@@ -1042,18 +1049,13 @@ template <typename T> struct Consumer<T, 18> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 8>(c, w, l); }
 };
 
-template <typename T, int KIND>
-__global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
-    fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+// The start every split kernel shares: the context, the ring's barriers, the
+// programmatic-dependent-launch wait, and the split's token range.
+template <int KIND>
+__device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const SplitParams& p,
+                                            const CUtensorMap* tmK, const CUtensorMap* tmV) {
     using Gm = Geo<KIND>;
     constexpr int kRing = Gm::kRing;
-    constexpr int kWarps = Gm::kWarps;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-
-    SplitCtx c;
     c.stages = kRing;
     c.p = &p;
     c.smem = smem;
@@ -1075,15 +1077,15 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
 #pragma unroll
         for (int s = 0; s < kRing; ++s) {
             mbar_init(c.full_bar(s), 1);
-            mbar_init(c.empty_bar(s), kWarps);
+            mbar_init(c.empty_bar(s), Gm::kEmptyArrivals);
         }
         *c.abort_flag = 0;
         *c.cons_abort = 0;
         fence_barrier_init();
     }
-    if (warp == kWarps && lane == 0) {
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
+    if (warp == Gm::kWarps && lane == 0) {
+        prefetch_tensormap(tmK);
+        prefetch_tensormap(tmV);
     }
     // Programmatic dependent launch: let the combine kernel that follows get
     // resident now, and wait for whatever preceded this kernel in the stream
@@ -1108,6 +1110,22 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     c.tok0 = u_begin * unit;
     c.tok1 = min((u_begin + u_count) * unit, L);
     c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Gm::kSub - 1) / Gm::kSub : 0;
+}
+
+template <typename T, int KIND>
+__global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
+    fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using Gm = Geo<KIND>;
+    constexpr int kWarps = Gm::kWarps;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SplitCtx c;
+    split_begin<KIND>(c, smem, p, &tmK, &tmV);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_splits;
     __syncthreads();
 
     if (warp == kWarps) {
@@ -1170,6 +1188,342 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 variant (KIND 31) for query blocks wider than 16 columns (16-bit
+// caches): one CTA serves all G * q_len (position, head) columns of a KV head,
+// up to 128, as the M rows of 5th-generation tensor-core MMAs with the
+// accumulators in tensor memory, instead of one CTA per 16 columns each
+// repeating the split's arithmetic on warp MMAs.
+//   S[col][tok]  = Q[col][:] . K[tok][:]        M = 128 columns, N = 64 tokens, K = 128 dims
+//   O[col][dim] += P[col][tok] . V[tok][dim]    M = 128, N = 128 dims, K = 64 tokens (V read MN-major)
+// Q (K-major, 128-byte swizzle) is staged once; K and V come from the TMA ring
+// exactly as for the 16-bit consumer.  S has two tensor-memory buffers (64
+// columns each), O one (128 columns).
+// Warps 0-7 run the online softmax (base 2): warp w reaches tensor-memory
+// lanes 32 (w % 4) .. +31, i.e. columns 32 (w % 4) .. +31, and takes tokens
+// 32 (w / 4) .. +31 of each stage, so the two warps of a lane quarter split a
+// stage's tokens and exchange their maxima through shared memory.  They write
+// P as hi + lo 16-bit parts into shared memory.  Warp 8 is the TMA producer;
+// one thread of warp 9 issues every MMA.  A column's running max moves only
+// when a stage's max exceeds it by more than 8 (log2 units), so p stays below
+// 2^8 and O is rescaled in tensor memory only then.  The states written at the
+// end are the same (u, m, l) as the other consumers'.
+// Shared memory: 4-stage ring (128 KB), Q (32 KB), P hi, P lo (16 KB each),
+// the softmax pairs' exchange (2 KB).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(Geo<31>::kThreads, 1)
+    fd_split_umma_kernel(const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using Gm = Geo<31>;
+    constexpr int kRing = Gm::kRing;
+    constexpr int kSoftmaxThreads = Gm::kWarps * 32;   // 256
+    constexpr uint32_t kTmemCols = 256;       // S0 [0, 64), S1 [64, 128), O [128, 256)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SplitCtx c;
+    split_begin<31>(c, smem, p, &tmK, &tmV);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_splits;
+    const int n_sub = c.n_sub;
+    // barriers after the ring's full[4] and empty[4]
+    const uint32_t b_s_full = c.bar0 + 64;    // [2], one arrival (MMA commit)
+    const uint32_t b_s_free = c.bar0 + 80;    // [2], one arrival per softmax warp
+    const uint32_t b_p_full = c.bar0 + 96;    // one arrival per softmax warp
+    const uint32_t b_p_free = c.bar0 + 104;   // one arrival (MMA commit): PV done
+    const uint32_t b_drain = c.bar0 + 112;    // one arrival (MMA commit): every MMA done
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Gm::kOffBars + 120);
+    uint8_t* sQ = smem + Gm::kOffExtra;       // two halves [128 x 64 dims]
+    uint8_t* sPh = sQ + 2 * 16384;            // [128 x 64 tokens]
+    uint8_t* sPl = sPh + 16384;
+    // the softmax pairs' exchange: stage maxima [stage parity][token half][column],
+    // final sums [token half][column], and one mbarrier per pair (lane quarter)
+    float* xmax = reinterpret_cast<float*>(sPl + 16384);
+    float* xsum = xmax + 512;
+    const uint32_t b_pair0 = smem_u32(xsum + 256);
+    if (threadIdx.x == 0) {
+        mbar_init(b_s_full, 1);
+        mbar_init(b_s_full + 8, 1);
+        mbar_init(b_s_free, Gm::kWarps);
+        mbar_init(b_s_free + 8, Gm::kWarps);
+        mbar_init(b_p_full, Gm::kWarps);
+        mbar_init(b_p_free, 1);
+        mbar_init(b_drain, 1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mbar_init(b_pair0 + 8u * q, 2);   // one arrival per warp of the pair
+        fence_barrier_init();
+    }
+    if (threadIdx.x < 128) {
+        // Q tile: row r is column r of the group (zeros past the columns)
+        const int r = threadIdx.x;
+        bool real;
+        const T* qrow = q_row<T>(c, r, real);
+        const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {
+            const uint4 v = real ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_o = tmem + 128;
+
+    if (warp == Gm::kWarps) {
+        produce<31>(c, &tmK, &tmV, lane);
+        return;
+    }
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+
+    if (warp == Gm::kWarps + 1) {
+        // ---- MMA issue: S of stage i + 1 goes out before PV of stage i, so
+        // the softmax of one stage overlaps the tensor cores' work on the next
+        if (lane == 0) {
+            const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
+            const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
+            const uint32_t q_addr = smem_u32(sQ);
+            auto issue_s = [&](int i) {
+                const uint32_t k_addr = smem_u32(c.smem + (i % kRing) * Gm::kStageBytes);
+                const uint32_t d = tmem + 64u * static_cast<uint32_t>(i & 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA
+                    const uint32_t off = (kk & 3) * 32u;   // 16 dims = 32 bytes inside a 128-byte row
+                    umma_f16(d, umma_desc_sw128(q_addr + (kk >> 2) * 16384u + off, 16, 1024),
+                             umma_desc_sw128(k_addr + (kk >> 2) * static_cast<uint32_t>(kHalfBytes) + off, 16, 1024),
+                             id_s, kk > 0);
+                }
+                umma_commit(b_s_full + 8u * static_cast<uint32_t>(i & 1));
+            };
+            bool ok = true;
+            if (n_sub > 0) {
+                ok = wait_or_flag(c.full_bar(0), 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                }
+            }
+            for (int i = 0; ok && i < n_sub; ++i) {
+                if (i + 1 < n_sub) {
+                    const int j = i + 1;
+                    ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
+                    if (ok && j >= 2) ok = wait_or_flag(b_s_free + 8u * (j & 1), ((j >> 1) - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j);
+                }
+                ok = wait_or_flag(b_p_full, i & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t v_addr = smem_u32(c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {   // P hi, then P lo
+                    const uint32_t p_addr = smem_u32(part ? sPl : sPh);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)       // 16 tokens per MMA
+                        umma_f16(tmem_o, umma_desc_sw128(p_addr + kk * 32u, 16, 1024),
+                                 umma_desc_sw128(v_addr + kk * 2048u, static_cast<uint32_t>(kHalfBytes), 1024),
+                                 id_o, i > 0 || part > 0 || kk > 0);
+                }
+                umma_commit(b_p_free);
+                umma_commit(c.empty_bar(i % kRing));
+            }
+            if (!ok) {
+                *c.cons_abort = 1;
+                *c.abort_flag = 1;
+            }
+            umma_commit(b_drain);              // tensor memory is freed only after this
+            wait_or_flag(b_drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warps: thread (w, lane) owns column r = 32 (w % 4) + lane
+        // (tensor-memory lane r) and tokens 32 h .. 32 h + 31 of each stage, h = w / 4
+        const int quarter = warp & 3, h = warp >> 2;
+        const int r = quarter * 32 + lane;
+        const bool quarter_active = quarter * 32 < p.cols;   // the pair's columns hold queries
+        const bool real = r < p.cols;
+        const int vis = real ? c.L - p.q_len + 1 + r / p.group : c.L;
+        const float sc = p.score_scale_log2;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t b_pair = b_pair0 + 8u * quarter;   // warps quarter and quarter + 4
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n_sub; ++i) {
+            const int buf = i & 1;
+            ok = __all_sync(kFull, wait_or_flag(b_s_full + 8u * buf, (i >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float t[32];
+            if (quarter_active) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + lane_base + 64u * buf + 32u * h + 16u * q, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) t[16 * q + e] = __uint_as_float(v[e]) * sc;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_s_free + 8u * buf);
+            const int tok = c.tok0 + i * Gm::kSub;
+            const int nvalid = min(Gm::kSub, c.tok1 - tok);
+            const bool partial = nvalid < Gm::kSub;
+            float alpha = 1.f;
+            bool need = false;
+            if (quarter_active) {
+                if (partial || tok + Gm::kSub > c.L - p.q_len + 1) {
+                    const int lim = min(nvalid, vis - tok) - 32 * h;   // in this warp's tokens
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (e >= lim) t[e] = -INFINITY;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, t[e]);
+                // the stage's max over both token halves, identical in both warps
+                // (double-buffered by stage parity: the partner has read the
+                // previous use of a slot before this warp passes the next exchange)
+                float* xm = xmax + (i & 1) * 256;
+                xm[h * 128 + r] = mx;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_pair);
+                ok = __all_sync(kFull, wait_or_flag(b_pair, i & 1));
+                if (!ok) break;
+                mx = fmaxf(mx, xm[(h ^ 1) * 128 + r]);
+                need = mx > m_run + 8.f;       // also true for the first finite max
+                if (need) {
+                    alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
+                    l_run *= alpha;
+                    m_run = mx;
+                }
+            }
+            if (i > 0) {   // PV of the previous stage done: P is free, O is settled
+                ok = __all_sync(kFull, wait_or_flag(b_p_free, (i - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                if (quarter_active && __any_sync(kFull, need)) {
+                    // this warp's half of the column's O row
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t v[16];
+                        const uint32_t ta = tmem_o + lane_base + 64u * h + 16u * q;
+                        tmem_ld16(ta, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st16(ta, v);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            if (quarter_active) {
+                const float mu = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {       // 8 tokens per 16-byte chunk
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = fast_exp2(t[8 * ch + 2 * e] - mu);
+                        const float p1 = fast_exp2(t[8 * ch + 2 * e + 1] - mu);
+                        l_run += p0 + p1;
+                        float k0, k1, d0, d1;
+                        hi[e] = Mma<T>::pack(p0, p1, k0, k1);
+                        lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
+                    }
+                    const int chunk = 4 * h + ch;
+                    const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            if (partial) {
+                // V rows past the end hold whatever the cache holds there; P is 0
+                // for them, but 0 * NaN would still poison PV
+                uint8_t* vb = c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes;
+                for (int idx = threadIdx.x; idx < (Gm::kSub - nvalid) * 16; idx += kSoftmaxThreads) {
+                    const int row = nvalid + (idx >> 4), ch = idx & 15;
+                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + row * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_full);
+        }
+        if (ok && n_sub > 0) {
+            ok = __all_sync(kFull, wait_or_flag(b_p_free, (n_sub - 1) & 1));
+            tc_fence_after();
+        }
+        if (!ok) *c.cons_abort = 1;
+        xsum[h * 128 + r] = l_run;
+        named_sync(1, kSoftmaxThreads);
+        if (*c.cons_abort == 0 && quarter_active) {
+            // the column's state (u, m, l), or out / lse directly with one split;
+            // this warp writes dims 64 h .. 64 h + 63
+            const float l_col = xsum[r] + xsum[128 + r];
+            const int64_t row = real ? (static_cast<int64_t>(c.b) * p.q_len + r / p.group) * p.n_q_heads +
+                                           c.kvh * p.group + r % p.group
+                                     : 0;
+            const float m_out = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
+            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t v[16];
+                if (n_sub > 0) {
+                    tmem_ld16(tmem_o + lane_base + 64u * h + 16u * q, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = 0u;
+                }
+                if (!real) continue;
+                const int d0 = 64 * h + 16 * q;
+                if (p.direct) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float o = empty ? 0.f : (__uint_as_float(v[e]) * p.v_scale) / l_col;
+                        const int64_t oi = row * kHeadDim + d0 + e;
+                        if (p.out_dtype == 2)
+                            static_cast<float*>(p.out)[oi] = o;
+                        else if (p.out_dtype == 0)
+                            static_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+                        else
+                            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.ws_u + (row * S + c.split) * kHeadDim + d0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_float4(__uint_as_float(v[4 * e]) * p.v_scale, __uint_as_float(v[4 * e + 1]) * p.v_scale,
+                                             __uint_as_float(v[4 * e + 2]) * p.v_scale, __uint_as_float(v[4 * e + 3]) * p.v_scale);
+                }
+            }
+            if (real && h == 0) {
+                if (p.direct) {
+                    if (p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l_col);
+                } else {
+                    p.ws_m[row * S + c.split] = m_out;
+                    p.ws_l[row * S + c.split] = l_col;
+                }
+            }
+        }
+    }
+    // every tensor-memory user is done (the MMA thread waited for its last commit)
+    tc_fence_before();
+    named_sync(2, kSoftmaxThreads + 32);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 template <typename T, int KIND>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
@@ -1191,9 +1545,15 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
 }
 
 template <typename T>
+static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
+                                    int batch, int n_kv_heads, cudaStream_t stream);
+
+template <typename T>
 static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                    const SplitParams& p, bool fp8, bool cuda_cores, int batch,
                                    int n_kv_heads, cudaStream_t stream) {
+    if (use_umma(fp8, cuda_cores, p.cols))
+        return launch_split_umma<T>(tmK, tmV, p, batch, n_kv_heads, stream);
     if (fp8)
         return p.cols <= 8 ? launch_split_t<T, 21>(tmK, tmV, p, batch, n_kv_heads, stream)
                            : launch_split_t<T, 22>(tmK, tmV, p, batch, n_kv_heads, stream);
@@ -1208,6 +1568,24 @@ static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tm
     }
     return p.cols <= 8 ? launch_split_t<T, 1>(tmK, tmV, p, batch, n_kv_heads, stream)
                        : launch_split_t<T, 2>(tmK, tmV, p, batch, n_kv_heads, stream);
+}
+
+template <typename T>
+static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
+                                    int batch, int n_kv_heads, cudaStream_t stream) {
+    auto kern = fd_split_umma_kernel<T>;
+    const size_t smem = Geo<31>::kSmem;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
+                      dim3(Geo<31>::kThreads), smem, stream, tmK, tmV, p);
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,

@@ -69,10 +69,8 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
         S = n_splits
     else:
         # the planner's rule with the CTAs per split of this query block
-        cols = (Hq // desc.n_kv_heads) * ql
-        cb = 1 if cols <= 8 else -(-cols // 16)
-        S = fd.fd_plan_splits(B * desc.n_kv_heads * cb, 2 * fd.fd_num_sms(),
-                              -(-int(seqlens_h.max()) // 128) if B else 0)
+        S = planned_splits(B, Hq, desc.n_kv_heads, ql, seqlens_h, fp8=desc.kv_dtype == fd.FD_E4M3,
+                           cuda_cores=(flags & fd.FD_FLAG_CUDA_CORES) != 0)
         if ql == 1:
             assert S == fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
     assert S >= 1
@@ -93,6 +91,18 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
     o = out.view.float().cpu().double().numpy().reshape(B * ql * Hq, D)
     l = lse.view.cpu().double().numpy()
     return o, l, S
+
+
+def planned_splits(B, Hq, Hkv, q_len, seqlens_h, fp8=False, cuda_cores=False):
+    """n_splits fd_decode plans: work = CTAs per split (column blocks of 16,
+    or one CTA of the tcgen05 variant for 16 < G*q_len <= 128 on a 16-bit
+    cache) x KV heads x batch, slots = 2 CTAs per SM (1 for tcgen05)."""
+    cols = (Hq // Hkv) * q_len
+    umma = not fp8 and not cuda_cores and 16 < cols <= 128
+    cb = 1 if (umma or cols <= 8) else -(-cols // 16)
+    per_sm = 1 if umma else 2
+    blocks = -(-int(np.max(seqlens_h)) // 128) if B else 0
+    return fd.fd_plan_splits(B * Hkv * cb, per_sm * fd.fd_num_sms(), blocks)
 
 
 def assert_parity(got_o, got_l, ref_o, ref_l, what=""):
