@@ -163,6 +163,16 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]^T: A's row r is tensor-memory lane r, two
+// 16-bit K elements per 32-bit column (the lower index in the low half).
+__device__ __forceinline__ void umma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate ? 1 : 0)
+                 : "memory");
+}
+
 // The mbarrier gets one arrival when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -162,12 +162,12 @@ struct Geo {
     static constexpr bool kF8 = KIND >= 20 && !kUmma;
     static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kUmma ? 8 : kConsumerWarps;
     static constexpr int kSub = kUmma ? 64 : 16 * kWarps;      // tokens per stage
-    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kUmma ? 4 : kStages;
+    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kUmma ? 5 : kStages;
     static constexpr int kTile = kSub * 128;                   // one box of 128-byte rows
     static constexpr int kStageBytes = (kF8 ? 2 : 4) * kTile;
-    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile, P hi, P lo
-    static constexpr int kExtraBytes = kUmma ? 2 * 16384 + 2 * 16384 + 4096 : 0;   // + softmax pair exchange
-    static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing] (+ tcgen05 barriers)
+    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile
+    static constexpr int kExtraBytes = kUmma ? 2 * 16384 + 4096 : 0;   // + exchange and tcgen05 barriers
+    static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing]
     static constexpr bool kOwnMap = kF8 || kUmma;
     static_assert(!kUmma || kSub == fdk::kSub, "the tcgen05 variant streams the 16-bit stages");
     static constexpr int kOffFlag = (kOwnMap ? kOffBars + 128 : fdk::kOffFlag);
@@ -178,7 +178,7 @@ struct Geo {
     // end-of-split merge area in stage memory: acc [warps][16][128], m, l [warps][16]
     static constexpr int kOffWM = kWarps * kCols * kHeadDim * 4;
     static constexpr int kOffWL = kOffWM + kWarps * kCols * 4;
-    static_assert(2 * kRing * 8 + (kUmma ? 6 * 8 + 8 : 0) <= 128, "barriers must fit");
+    static_assert(2 * kRing * 8 <= 128, "barriers must fit");
     static_assert(kOffWL + kWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
     static_assert(kOwnMap || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
                               kOffBars == fdk::kOffBars), "16-bit variants use the map above");
@@ -1196,20 +1196,22 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
 // repeating the split's arithmetic on warp MMAs.
 //   S[col][tok]  = Q[col][:] . K[tok][:]        M = 128 columns, N = 64 tokens, K = 128 dims
 //   O[col][dim] += P[col][tok] . V[tok][dim]    M = 128, N = 128 dims, K = 64 tokens (V read MN-major)
-// Q (K-major, 128-byte swizzle) is staged once; K and V come from the TMA ring
-// exactly as for the 16-bit consumer.  S has two tensor-memory buffers (64
-// columns each), O one (128 columns).
+// Q (K-major, 128-byte swizzle) is staged once in shared memory; K and V come
+// from the TMA ring exactly as for the 16-bit consumer.  P never leaves the
+// tensor memory: the softmax stores it there (hi + lo 16-bit parts, two per
+// 32-bit column) and PV takes it as its A operand.  Tensor memory holds two S
+// buffers and two P buffers (64 columns each) and O (128 columns), so the
+// softmax of stage i + 1 overlaps PV of stage i.
 // Warps 0-7 run the online softmax (base 2): warp w reaches tensor-memory
 // lanes 32 (w % 4) .. +31, i.e. columns 32 (w % 4) .. +31, and takes tokens
 // 32 (w / 4) .. +31 of each stage, so the two warps of a lane quarter split a
-// stage's tokens and exchange their maxima through shared memory.  They write
-// P as hi + lo 16-bit parts into shared memory.  Warp 8 is the TMA producer;
-// one thread of warp 9 issues every MMA.  A column's running max moves only
-// when a stage's max exceeds it by more than 8 (log2 units), so p stays below
-// 2^8 and O is rescaled in tensor memory only then.  The states written at the
-// end are the same (u, m, l) as the other consumers'.
-// Shared memory: 4-stage ring (128 KB), Q (32 KB), P hi, P lo (16 KB each),
-// the softmax pairs' exchange (2 KB).
+// stage's tokens and exchange their maxima through shared memory.  Warp 8 is
+// the TMA producer; one thread of warp 9 issues every MMA.  A column's running
+// max moves only when a stage's max exceeds it by more than 8 (log2 units),
+// so p stays below 2^8 and O is rescaled in tensor memory only then.  The
+// states written at the end are the same (u, m, l) as the other consumers'.
+// Shared memory: 5-stage ring (160 KB), Q (32 KB), the softmax pairs'
+// exchange and the tcgen05 barriers (4 KB).
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
@@ -1218,7 +1220,8 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     using Gm = Geo<31>;
     constexpr int kRing = Gm::kRing;
     constexpr int kSoftmaxThreads = Gm::kWarps * 32;   // 256
-    constexpr uint32_t kTmemCols = 256;       // S0 [0, 64), S1 [64, 128), O [128, 256)
+    // S [0, 128) and P [128, 256) double-buffered by stage parity, O [256, 384)
+    constexpr uint32_t kTmemCols = 512;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1228,31 +1231,30 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
     const int n_sub = c.n_sub;
-    // barriers after the ring's full[4] and empty[4]
-    const uint32_t b_s_full = c.bar0 + 64;    // [2], one arrival (MMA commit)
-    const uint32_t b_s_free = c.bar0 + 80;    // [2], one arrival per softmax warp
-    const uint32_t b_p_full = c.bar0 + 96;    // one arrival per softmax warp
-    const uint32_t b_p_free = c.bar0 + 104;   // one arrival (MMA commit): PV done
-    const uint32_t b_drain = c.bar0 + 112;    // one arrival (MMA commit): every MMA done
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Gm::kOffBars + 120);
     uint8_t* sQ = smem + Gm::kOffExtra;       // two halves [128 x 64 dims]
-    uint8_t* sPh = sQ + 2 * 16384;            // [128 x 64 tokens]
-    uint8_t* sPl = sPh + 16384;
     // the softmax pairs' exchange: stage maxima [stage parity][token half][column],
-    // final sums [token half][column], and one mbarrier per pair (lane quarter)
-    float* xmax = reinterpret_cast<float*>(sPl + 16384);
+    // final sums [token half][column]
+    float* xmax = reinterpret_cast<float*>(sQ + 2 * 16384);
     float* xsum = xmax + 512;
-    const uint32_t b_pair0 = smem_u32(xsum + 256);
+    // mbarriers, each [2] by stage parity except drain and the pairs'
+    const uint32_t b_pair0 = smem_u32(xsum + 256);   // [4], one per lane quarter: one arrival per warp of the pair
+    const uint32_t b_s_full = b_pair0 + 32;   // one arrival (MMA commit): S written
+    const uint32_t b_s_free = b_pair0 + 48;   // one arrival per softmax warp: S read
+    const uint32_t b_p_full = b_pair0 + 64;   // one arrival per softmax warp: P written (and O rescaled)
+    const uint32_t b_o_done = b_pair0 + 80;   // one arrival (MMA commit): PV done
+    const uint32_t b_drain = b_pair0 + 96;    // one arrival (MMA commit): every MMA done
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(xsum + 256 + 26);   // b_pair0 + 104
     if (threadIdx.x == 0) {
-        mbar_init(b_s_full, 1);
-        mbar_init(b_s_full + 8, 1);
-        mbar_init(b_s_free, Gm::kWarps);
-        mbar_init(b_s_free + 8, Gm::kWarps);
-        mbar_init(b_p_full, Gm::kWarps);
-        mbar_init(b_p_free, 1);
-        mbar_init(b_drain, 1);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) mbar_init(b_pair0 + 8u * q, 2);   // one arrival per warp of the pair
+        for (int q = 0; q < 4; ++q) mbar_init(b_pair0 + 8u * q, 2);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_s_full + 8u * b, 1);
+            mbar_init(b_s_free + 8u * b, Gm::kWarps);
+            mbar_init(b_p_full + 8u * b, Gm::kWarps);
+            mbar_init(b_o_done + 8u * b, 1);
+        }
+        mbar_init(b_drain, 1);
         fence_barrier_init();
     }
     if (threadIdx.x < 128) {
@@ -1273,7 +1275,8 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 128;
+    const uint32_t tmem_p = tmem + 128;
+    const uint32_t tmem_o = tmem + 256;
 
     if (warp == Gm::kWarps) {
         produce<31>(c, &tmK, &tmV, lane);
@@ -1285,18 +1288,23 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
         // ---- MMA issue: S of stage i + 1 goes out before PV of stage i, so
         // the softmax of one stage overlaps the tensor cores' work on the next
         if (lane == 0) {
+            // Issue cost bounds this thread: each descriptor is built once and
+            // offset by constants (the start address is the low field, in
+            // 16-byte units, and no operand crosses 256 KB, so adding never carries).
             const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
             const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
-            const uint32_t q_addr = smem_u32(sQ);
+            const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = umma_desc_sw128(smem_u32(c.smem), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(c.smem + 2 * kHalfBytes), static_cast<uint32_t>(kHalfBytes), 1024);
+            constexpr uint32_t kStageUnits = Gm::kStageBytes >> 4;
             auto issue_s = [&](int i) {
-                const uint32_t k_addr = smem_u32(c.smem + (i % kRing) * Gm::kStageBytes);
+                const uint64_t dk = dk0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
                 const uint32_t d = tmem + 64u * static_cast<uint32_t>(i & 1);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA
-                    const uint32_t off = (kk & 3) * 32u;   // 16 dims = 32 bytes inside a 128-byte row
-                    umma_f16(d, umma_desc_sw128(q_addr + (kk >> 2) * 16384u + off, 16, 1024),
-                             umma_desc_sw128(k_addr + (kk >> 2) * static_cast<uint32_t>(kHalfBytes) + off, 16, 1024),
-                             id_s, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA: 32 bytes inside a 128-byte row
+                    const uint32_t q_off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                    const uint32_t k_off = ((kk >> 2) * static_cast<uint32_t>(kHalfBytes) + (kk & 3) * 32u) >> 4;
+                    umma_f16(d, dq + q_off, dk + k_off, id_s, kk > 0);
                 }
                 umma_commit(b_s_full + 8u * static_cast<uint32_t>(i & 1));
             };
@@ -1317,20 +1325,22 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     tc_fence_after();
                     issue_s(j);
                 }
-                ok = wait_or_flag(b_p_full, i & 1);
+                ok = wait_or_flag(b_p_full + 8u * (i & 1), (i >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes);
+                const uint64_t dv = dv0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
+                const uint32_t pa = tmem_p + 64u * static_cast<uint32_t>(i & 1);
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {   // P hi, then P lo
-                    const uint32_t p_addr = smem_u32(part ? sPl : sPh);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)       // 16 tokens per MMA
-                        umma_f16(tmem_o, umma_desc_sw128(p_addr + kk * 32u, 16, 1024),
-                                 umma_desc_sw128(v_addr + kk * 2048u, static_cast<uint32_t>(kHalfBytes), 1024),
-                                 id_o, i > 0 || part > 0 || kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {     // 16 tokens (two 8-row groups) per MMA
+                        // tokens 16 kk .. +15 were written by the warps of token half kk / 2:
+                        // hi at columns 32 (kk / 2) + 8 (kk % 2), lo 16 columns further
+                        const uint32_t a = pa + 32u * (kk >> 1) + 16u * part + 8u * (kk & 1);
+                        umma_f16_ta(tmem_o, a, dv + ((kk * 2048u) >> 4), id_o, i > 0 || part > 0 || kk > 0);
+                    }
                 }
-                umma_commit(b_p_free);
+                umma_commit(b_o_done + 8u * static_cast<uint32_t>(i & 1));
                 umma_commit(c.empty_bar(i % kRing));
             }
             if (!ok) {
@@ -1378,6 +1388,7 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
             const bool partial = nvalid < Gm::kSub;
             float alpha = 1.f;
             bool need = false;
+            uint32_t hi[16], lo[16];
             if (quarter_active) {
                 if (partial || tok + Gm::kSub > c.L - p.q_len + 1) {
                     const int lim = min(nvalid, vis - tok) - 32 * h;   // in this warp's tokens
@@ -1404,12 +1415,33 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     l_run *= alpha;
                     m_run = mx;
                 }
+                const float mu = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = fast_exp2(t[2 * e] - mu);
+                    const float p1 = fast_exp2(t[2 * e + 1] - mu);
+                    l_run += p0 + p1;
+                    float k0, k1, d0, d1;
+                    hi[e] = Mma<T>::pack(p0, p1, k0, k1);
+                    lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
+                }
             }
-            if (i > 0) {   // PV of the previous stage done: P is free, O is settled
-                ok = __all_sync(kFull, wait_or_flag(b_p_free, (i - 1) & 1));
+            if (i >= 2) {   // PV of stage i - 2 has read this P buffer
+                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * buf, ((i >> 1) - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                if (quarter_active && __any_sync(kFull, need)) {
+            }
+            if (quarter_active) {
+                // this warp's 32 tokens: hi in its first 16 columns, lo in the next 16
+                const uint32_t pa = tmem_p + lane_base + 64u * buf + 32u * h;
+                tmem_st16(pa, hi);
+                tmem_st16(pa + 16u, lo);
+            }
+            if (i > 0 && quarter_active && __any_sync(kFull, need)) {
+                // O is rescaled once PV of stage i - 1 is done with it
+                const bool done = __all_sync(kFull, wait_or_flag(b_o_done + 8u * (buf ^ 1), ((i - 1) >> 1) & 1));
+                if (done) {
+                    tc_fence_after();
                     // this warp's half of the column's O row
 #pragma unroll 1
                     for (int q = 0; q < 4; ++q) {
@@ -1421,29 +1453,11 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                         for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                         tmem_st16(ta, v);
                     }
-                    tmem_wait_st();
                 }
+                ok = done;
             }
-            if (quarter_active) {
-                const float mu = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {       // 8 tokens per 16-byte chunk
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = fast_exp2(t[8 * ch + 2 * e] - mu);
-                        const float p1 = fast_exp2(t[8 * ch + 2 * e + 1] - mu);
-                        l_run += p0 + p1;
-                        float k0, k1, d0, d1;
-                        hi[e] = Mma<T>::pack(p0, p1, k0, k1);
-                        lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
-                    }
-                    const int chunk = 4 * h + ch;
-                    const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-            }
+            tmem_wait_st();
+            if (!ok) break;
             if (partial) {
                 // V rows past the end hold whatever the cache holds there; P is 0
                 // for them, but 0 * NaN would still poison PV
@@ -1453,14 +1467,14 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + row * 128 + ((ch & 7) << 4)) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_p_full);
+            if (lane == 0) mbar_arrive(b_p_full + 8u * buf);
         }
-        if (ok && n_sub > 0) {
-            ok = __all_sync(kFull, wait_or_flag(b_p_free, (n_sub - 1) & 1));
+        if (ok && n_sub > 0) {   // the last PV done (it completes after every earlier one)
+            ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * ((n_sub - 1) & 1), ((n_sub - 1) >> 1) & 1));
             tc_fence_after();
         }
         if (!ok) *c.cons_abort = 1;
