@@ -158,15 +158,16 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 // holds 96 KB, and two CTAs fit on an SM.
 template <int KIND>
 struct Geo {
-    static constexpr bool kUmma = KIND == 31;                  // tcgen05 consumer, see below
+    static constexpr bool kUmma = KIND == 31 || KIND == 32;    // tcgen05 consumers, see below
     static constexpr bool kF8 = KIND >= 20 && !kUmma;
     static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kUmma ? 8 : kConsumerWarps;
     static constexpr int kSub = kUmma ? 64 : 16 * kWarps;      // tokens per stage
-    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kUmma ? 5 : kStages;
+    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : KIND == 31 ? 5 : KIND == 32 ? 4 : kStages;
     static constexpr int kTile = kSub * 128;                   // one box of 128-byte rows
     static constexpr int kStageBytes = (kF8 ? 2 : 4) * kTile;
-    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile
-    static constexpr int kExtraBytes = kUmma ? 2 * 16384 + 4096 : 0;   // + exchange and tcgen05 barriers
+    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile (and P, KIND 32)
+    // + the softmax exchange and the tcgen05 barriers (4 KB)
+    static constexpr int kExtraBytes = KIND == 31 ? 2 * 16384 + 4096 : KIND == 32 ? 4 * 16384 + 4096 : 0;
     static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing]
     static constexpr bool kOwnMap = kF8 || kUmma;
     static_assert(!kUmma || kSub == fdk::kSub, "the tcgen05 variant streams the 16-bit stages");
@@ -1538,6 +1539,360 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 variant for 17-64 columns (KIND 32).  Every tcgen05.mma costs the
+// tensor pipe about the same time up to N = 128, so this variant fills the
+// M = 128 rows twice over instead of leaving half of them empty:
+//   Q rows 64 + c repeat rows c, so S lanes 64 + c repeat the scores of column c;
+//   P rows 0..63 hold the hi parts of the columns' weights, rows 64..127 the lo parts,
+//   and one MMA per 16 tokens accumulates O rows c (hi) and 64 + c (lo) together.
+// PV takes 4 MMAs per stage instead of 8, and the result is O[c] = O[c] + O[64 + c]
+// at the end.  Each column is served by four softmax warps (both lane quarters
+// that hold its scores, two warps each), each taking 16 of a stage's 64 tokens;
+// the four exchange their maxima every stage, so all four track the same
+// running max and each rescales its own O rows when it moves.  P is written to
+// shared memory (K-major, 128-byte swizzle), double-buffered by stage parity.
+// Shared memory: 4-stage ring (128 KB), Q (32 KB), P (2 x 16 KB), the
+// exchange and the tcgen05 barriers (4 KB).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(Geo<32>::kThreads, 1)
+    fd_split_umma64_kernel(const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using Gm = Geo<32>;
+    constexpr int kRing = Gm::kRing;
+    constexpr int kSoftmaxThreads = Gm::kWarps * 32;   // 256
+    constexpr uint32_t kTmemCols = 256;       // S [0, 128) double-buffered by stage parity, O [128, 256)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SplitCtx c;
+    split_begin<32>(c, smem, p, &tmK, &tmV);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_splits;
+    const int n_sub = c.n_sub;
+    uint8_t* sQ = smem + Gm::kOffExtra;       // two halves [128 x 64 dims]
+    uint8_t* sP = sQ + 2 * 16384;             // [stage parity][128 rows x 64 tokens]
+    // the exchange: stage maxima [stage parity][token quarter][column], sums [token quarter][column]
+    float* xmax = reinterpret_cast<float*>(sP + 2 * 16384);
+    float* xsum = xmax + 512;
+    // mbarriers, [2] by stage parity unless noted
+    const uint32_t b_grp0 = smem_u32(xsum + 256);   // [2], one per column group: one arrival per warp of its four
+    const uint32_t b_s_full = b_grp0 + 16;    // one arrival (MMA commit): S written
+    const uint32_t b_s_free = b_grp0 + 32;    // one arrival per softmax warp: S read
+    const uint32_t b_p_full = b_grp0 + 48;    // one arrival per softmax warp: P written (and O rescaled)
+    const uint32_t b_o_done = b_grp0 + 64;    // one arrival (MMA commit): PV done
+    const uint32_t b_drain = b_grp0 + 80;     // single, one arrival (MMA commit): every MMA done
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(xsum + 256 + 22);   // b_grp0 + 88
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_grp0 + 8u * b, 4);
+            mbar_init(b_s_full + 8u * b, 1);
+            mbar_init(b_s_free + 8u * b, Gm::kWarps);
+            mbar_init(b_p_full + 8u * b, Gm::kWarps);
+            mbar_init(b_o_done + 8u * b, 1);
+        }
+        mbar_init(b_drain, 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x < 128) {
+        // Q tile: rows r and 64 + r are column r of the group (zeros past the columns)
+        const int r = threadIdx.x;
+        bool real;
+        const T* qrow = q_row<T>(c, r & 63, real);
+        const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {
+            const uint4 v = real ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_o = tmem + 128;
+
+    if (warp == Gm::kWarps) {
+        produce<32>(c, &tmK, &tmV, lane);
+        return;
+    }
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+
+    if (warp == Gm::kWarps + 1) {
+        // ---- MMA issue (one thread): S of stage i + 1 goes out before PV of stage i.
+        // Each descriptor is built once and offset by constants (the start address
+        // is the low field, in 16-byte units, and no operand crosses 256 KB).
+        if (lane == 0) {
+            const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
+            const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
+            const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dp0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
+            const uint64_t dk0 = umma_desc_sw128(smem_u32(c.smem), 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(c.smem + 2 * kHalfBytes), static_cast<uint32_t>(kHalfBytes), 1024);
+            constexpr uint32_t kStageUnits = Gm::kStageBytes >> 4;
+            auto issue_s = [&](int i) {
+                const uint64_t dk = dk0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
+                const uint32_t d = tmem + 64u * static_cast<uint32_t>(i & 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA: 32 bytes inside a 128-byte row
+                    const uint32_t q_off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                    const uint32_t k_off = ((kk >> 2) * static_cast<uint32_t>(kHalfBytes) + (kk & 3) * 32u) >> 4;
+                    umma_f16(d, dq + q_off, dk + k_off, id_s, kk > 0);
+                }
+                umma_commit(b_s_full + 8u * static_cast<uint32_t>(i & 1));
+            };
+            bool ok = true;
+            if (n_sub > 0) {
+                ok = wait_or_flag(c.full_bar(0), 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                }
+            }
+            for (int i = 0; ok && i < n_sub; ++i) {
+                if (i + 1 < n_sub) {
+                    const int j = i + 1;
+                    ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
+                    if (ok && j >= 2) ok = wait_or_flag(b_s_free + 8u * (j & 1), ((j >> 1) - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j);
+                }
+                ok = wait_or_flag(b_p_full + 8u * (i & 1), (i >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dv = dv0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
+                const uint64_t dp = dp0 + static_cast<uint32_t>(i & 1) * (16384u >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // 16 tokens per MMA: hi and lo rows together
+                    umma_f16(tmem_o, dp + ((kk * 32u) >> 4), dv + ((kk * 2048u) >> 4), id_o, i > 0 || kk > 0);
+                umma_commit(b_o_done + 8u * static_cast<uint32_t>(i & 1));
+                umma_commit(c.empty_bar(i % kRing));
+            }
+            if (!ok) {
+                *c.cons_abort = 1;
+                *c.abort_flag = 1;
+            }
+            umma_commit(b_drain);              // tensor memory is freed only after this
+            wait_or_flag(b_drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warps.  Warp w reaches tensor-memory lanes 32 q .. +31,
+        // q = w % 4: the scores (and O rows) of columns col = 32 (q % 2) + lane,
+        // the hi rows for q < 2 and the lo rows for q >= 2.  Its tokens are
+        // 16 tq .. 16 tq + 15 of each stage, tq = 2 (q / 2) + w / 4, and its O
+        // dims are 64 (w / 4) .. +63.  Column group g = q % 2 has the four warps
+        // g, g + 2, g + 4, g + 6.
+        const int q = warp & 3, hw = warp >> 2;
+        const int g = q & 1, side = q >> 1;
+        const int col = 32 * g + lane;
+        const int tq = 2 * side + hw;
+        const bool group_active = 32 * g < p.cols;
+        const bool real = col < p.cols;
+        const int vis = real ? c.L - p.q_len + 1 + col / p.group : c.L;
+        const float sc = p.score_scale_log2;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t b_grp = b_grp0 + 8u * g;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n_sub; ++i) {
+            const int buf = i & 1;
+            ok = __all_sync(kFull, wait_or_flag(b_s_full + 8u * buf, (i >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float t[16];
+            if (group_active) {
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base + 64u * buf + 16u * tq, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(v[e]) * sc;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_s_free + 8u * buf);
+            const int tok = c.tok0 + i * Gm::kSub;
+            const int nvalid = min(Gm::kSub, c.tok1 - tok);
+            const bool partial = nvalid < Gm::kSub;
+            float alpha = 1.f;
+            bool need = false;
+            uint32_t hi[8], lo[8];
+            if (group_active) {
+                if (partial || tok + Gm::kSub > c.L - p.q_len + 1) {
+                    const int lim = min(nvalid, vis - tok) - 16 * tq;   // in this warp's tokens
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (e >= lim) t[e] = -INFINITY;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) mx = fmaxf(mx, t[e]);
+                // the stage's max over the four token quarters, identical in the
+                // group's four warps (double-buffered by stage parity: every warp
+                // has read a slot before the group passes its next exchange)
+                float* xm = xmax + (i & 1) * 256;
+                xm[tq * 64 + col] = mx;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_grp);
+                ok = __all_sync(kFull, wait_or_flag(b_grp, i & 1));
+                if (!ok) break;
+                mx = fmaxf(fmaxf(xm[col], xm[64 + col]), fmaxf(xm[128 + col], xm[192 + col]));
+                need = mx > m_run + 8.f;       // also true for the first finite max
+                if (need) {
+                    alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
+                    l_run *= alpha;
+                    m_run = mx;
+                }
+                const float mu = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float p0 = fast_exp2(t[2 * e] - mu);
+                    const float p1 = fast_exp2(t[2 * e + 1] - mu);
+                    l_run += p0 + p1;
+                    float k0, k1, d0, d1;
+                    hi[e] = Mma<T>::pack(p0, p1, k0, k1);
+                    lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
+                }
+            }
+            if (i >= 2) {   // PV of stage i - 2 has read this P buffer
+                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * buf, ((i >> 1) - 1) & 1));
+                if (!ok) break;
+            }
+            if (group_active) {
+                // tokens 16 tq .. +15 = chunks 2 tq, 2 tq + 1 of rows col (hi) and 64 + col (lo)
+                uint8_t* pb = sP + buf * 16384;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int chunk = 2 * tq + h2;
+                    const int rh = col, rl = 64 + col;
+                    *reinterpret_cast<uint4*>(pb + rh * 128 + ((chunk ^ (rh & 7)) << 4)) =
+                        make_uint4(hi[4 * h2], hi[4 * h2 + 1], hi[4 * h2 + 2], hi[4 * h2 + 3]);
+                    *reinterpret_cast<uint4*>(pb + rl * 128 + ((chunk ^ (rl & 7)) << 4)) =
+                        make_uint4(lo[4 * h2], lo[4 * h2 + 1], lo[4 * h2 + 2], lo[4 * h2 + 3]);
+                }
+            }
+            if (i > 0 && group_active && __any_sync(kFull, need)) {
+                // O is rescaled once PV of stage i - 1 is done with it: this warp's
+                // 32 O rows, dims 64 hw .. +63
+                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * (buf ^ 1), ((i - 1) >> 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int qq = 0; qq < 4; ++qq) {
+                    uint32_t v[16];
+                    const uint32_t ta = tmem_o + lane_base + 64u * hw + 16u * qq;
+                    tmem_ld16(ta, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st16(ta, v);
+                }
+                tmem_wait_st();
+            }
+            if (partial) {
+                // V rows past the end hold whatever the cache holds there; P is 0
+                // for them, but 0 * NaN would still poison PV
+                uint8_t* vb = c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes;
+                for (int idx = threadIdx.x; idx < (Gm::kSub - nvalid) * 16; idx += kSoftmaxThreads) {
+                    const int row = nvalid + (idx >> 4), ch = idx & 15;
+                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + row * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_full + 8u * buf);
+        }
+        if (ok && n_sub > 0) {   // the last PV done (it completes after every earlier one)
+            ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * ((n_sub - 1) & 1), ((n_sub - 1) >> 1) & 1));
+            tc_fence_after();
+        }
+        if (!ok) *c.cons_abort = 1;
+        xsum[tq * 64 + col] = l_run;
+        // the lo rows of O go through shared memory (ring stage 0, idle now):
+        // [64 columns][128 dims] fp32
+        float* olo = reinterpret_cast<float*>(c.smem);
+        if (ok && side == 1 && group_active && n_sub > 0) {
+#pragma unroll 1
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t v[16];
+                tmem_ld16(tmem_o + lane_base + 64u * hw + 16u * qq, v);
+                tmem_wait_ld();
+                float4* dst = reinterpret_cast<float4*>(olo + col * kHeadDim + 64 * hw + 16 * qq);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            }
+        }
+        named_sync(1, kSoftmaxThreads);
+        if (*c.cons_abort == 0 && side == 0 && group_active) {
+            // the column's state (u, m, l), or out / lse directly with one split;
+            // this warp writes dims 64 hw .. 64 hw + 63
+            const float l_col = (xsum[col] + xsum[64 + col]) + (xsum[128 + col] + xsum[192 + col]);
+            const int64_t row = real ? (static_cast<int64_t>(c.b) * p.q_len + col / p.group) * p.n_q_heads +
+                                           c.kvh * p.group + col % p.group
+                                     : 0;
+            const float m_out = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
+            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
+#pragma unroll 1
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t v[16];
+                if (n_sub > 0) {
+                    tmem_ld16(tmem_o + lane_base + 64u * hw + 16u * qq, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = 0u;
+                }
+                if (!real) continue;
+                const int d0 = 64 * hw + 16 * qq;
+                float o[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    o[e] = n_sub > 0 ? (__uint_as_float(v[e]) + olo[col * kHeadDim + d0 + e]) * p.v_scale : 0.f;
+                if (p.direct) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float y = empty ? 0.f : o[e] / l_col;
+                        const int64_t oi = row * kHeadDim + d0 + e;
+                        if (p.out_dtype == 2)
+                            static_cast<float*>(p.out)[oi] = y;
+                        else if (p.out_dtype == 0)
+                            static_cast<__half*>(p.out)[oi] = __float2half_rn(y);
+                        else
+                            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(y);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.ws_u + (row * S + c.split) * kHeadDim + d0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                }
+            }
+            if (real && hw == 0) {
+                if (p.direct) {
+                    if (p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l_col);
+                } else {
+                    p.ws_m[row * S + c.split] = m_out;
+                    p.ws_l[row * S + c.split] = l_col;
+                }
+            }
+        }
+    }
+    // every tensor-memory user is done (the MMA thread waited for its last commit)
+    tc_fence_before();
+    named_sync(2, kSoftmaxThreads + 32);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 template <typename T, int KIND>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
@@ -1558,7 +1913,7 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
                       dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
-template <typename T>
+template <typename T, int KIND>
 static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
                                     int batch, int n_kv_heads, cudaStream_t stream);
 
@@ -1567,7 +1922,8 @@ static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tm
                                    const SplitParams& p, bool fp8, bool cuda_cores, int batch,
                                    int n_kv_heads, cudaStream_t stream) {
     if (use_umma(fp8, cuda_cores, p.cols))
-        return launch_split_umma<T>(tmK, tmV, p, batch, n_kv_heads, stream);
+        return p.cols <= 64 ? launch_split_umma<T, 32>(tmK, tmV, p, batch, n_kv_heads, stream)
+                            : launch_split_umma<T, 31>(tmK, tmV, p, batch, n_kv_heads, stream);
     if (fp8)
         return p.cols <= 8 ? launch_split_t<T, 21>(tmK, tmV, p, batch, n_kv_heads, stream)
                            : launch_split_t<T, 22>(tmK, tmV, p, batch, n_kv_heads, stream);
@@ -1584,11 +1940,11 @@ static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tm
                        : launch_split_t<T, 2>(tmK, tmV, p, batch, n_kv_heads, stream);
 }
 
-template <typename T>
+template <typename T, int KIND>
 static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
                                     int batch, int n_kv_heads, cudaStream_t stream) {
-    auto kern = fd_split_umma_kernel<T>;
-    const size_t smem = Geo<31>::kSmem;
+    auto kern = KIND == 32 ? fd_split_umma64_kernel<T> : fd_split_umma_kernel<T>;
+    const size_t smem = Geo<KIND>::kSmem;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1599,7 +1955,7 @@ static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& 
         configured_device = dev;
     }
     return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
-                      dim3(Geo<31>::kThreads), smem, stream, tmK, tmV, p);
+                      dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,

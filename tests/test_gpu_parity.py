@@ -536,6 +536,35 @@ def test_query_blocks(q_len, group):
         assert_parity(got_o, got_l, ref_o, ref_l, f"q_len={q_len} G={group} S={S}")
 
 
+@pytest.mark.parametrize("group,q_len,dtype", [(12, 6, "bf16"), (5, 16, "f16"), (16, 8, "bf16"),
+                                               (9, 16, "f16"), (16, 16, "bf16")])
+def test_query_blocks_wide(group, q_len, dtype):
+    """Query blocks of 72, 80 and 128 columns (one tcgen05 CTA serves a KV
+    head's whole group) and of 144 and 256 columns (column blocks of 16),
+    against the oracle; one sequence shorter than the block."""
+    B, Hkv, D, T = 2, 2, 128, 900
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, q_len, Hq, D), dtype, 1450 + 10 * q_len + group, device=DEV)
+    k, v = _cache(B, Hkv, T, D, dtype, 1550 + group)
+    sl = np.array([900, 11], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
+    for S in (0, 1, 5):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"q_len={q_len} G={group} S={S}")
+
+
+def test_query_block_wide_paged():
+    """A paged 128-column block (G = 16, q_len = 8) on the tcgen05 path."""
+    B, Hkv, G, D, ps, ql = 2, 2, 16, 128, 64, 8
+    lens = [1500, 333]
+    pk, pv, bt = _paged_problem(B, Hkv, D, ps, lens, "bf16", 1603)
+    q = fd_inputs.randn((B, ql, Hkv * G, D), "bf16", 1604, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "bf16", Hkv, page_size=ps, block_table=bt)
+    assert_parity(got_o, got_l, ref_o, ref_l, "paged wide query block")
+
+
 def test_query_block_paged_and_strided():
     B, Hkv, G, D, ps, ql = 2, 4, 4, 128, 16, 4
     lens = [2049, 700]
