@@ -59,7 +59,8 @@ def _args():
                     help="use the CUDA-core consumer of fd_split instead of the tensor-core one")
     ap.add_argument("--workload", default=None,
                     choices=["tiny_mha", "long_gqa_128k", "varlen_b16", "paged_b8", "sweep",
-                             "query_block_q4", "long_gqa_128k_fp8", "sweep_fp8"],
+                             "query_block_q4", "query_block_g8_q4", "query_block_g8_q8",
+                             "query_block_g16_q8", "long_gqa_128k_fp8", "sweep_fp8"],
                     help="time one workload (one JSON line per problem) instead of the default line")
     return ap.parse_args()
 

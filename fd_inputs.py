@@ -19,6 +19,9 @@ Workloads (the pages measure on no dataset; every input is synthetic):
                  heads, d=128, fp16.
   query_block_q4 B=4, 32 / 8 heads, d=128, bf16, 32768 tokens, 4 query
                  positions per sequence (a speculative-verification block).
+  query_block_g8_q4, query_block_g8_q8, query_block_g16_q8  the same cache
+                 with 64 or 128 query heads and 4 or 8 positions: 32, 64 and
+                 128 (position, head) columns per KV head.
   long_gqa_128k_fp8  the headline shape with an E4M3 cache (q fp16), values
                  stored x64 with k_scale = v_scale = 1/64.
   sweep_fp8     the sweep's grid over such an E4M3 cache.
@@ -52,6 +55,14 @@ WORKLOADS = {
     # short query block (speculative verification of 4 draft tokens)
     "query_block_q4": dict(batch=4, n_q_heads=32, n_kv_heads=8, head_dim=128, ctx=32768,
                            q_len=4, dtype="bf16", seed=1006),
+    # wider blocks: a group of 8 query heads per KV head, 4 or 8 positions
+    # (32 and 64 columns per KV head), and 16 heads x 8 positions (128 columns)
+    "query_block_g8_q4": dict(batch=4, n_q_heads=64, n_kv_heads=8, head_dim=128, ctx=32768,
+                              q_len=4, dtype="bf16", seed=1009),
+    "query_block_g8_q8": dict(batch=4, n_q_heads=64, n_kv_heads=8, head_dim=128, ctx=32768,
+                              q_len=8, dtype="bf16", seed=1010),
+    "query_block_g16_q8": dict(batch=4, n_q_heads=128, n_kv_heads=8, head_dim=128, ctx=32768,
+                               q_len=8, dtype="bf16", seed=1011),
 }
 
 
