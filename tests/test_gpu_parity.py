@@ -450,30 +450,35 @@ def test_lse_chaining_two_halves_merged_externally():
     np.testing.assert_allclose(got_l, l_full, rtol=0, atol=2e-5)
 
 
-@pytest.mark.parametrize("kind", ["f16", "e4m3"])
+@pytest.mark.parametrize("kind", ["f16", "e4m3", "f16_g8_q4", "bf16_g16_q8"])
 def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     """The test hook drops the first K/V stage: the kernel's bounded wait runs
     out, the status word reports FD_ERR_DEVICE_TIMEOUT, nothing faults, and
-    the next call on the same context is correct.  Both the 16-bit consumer
-    and the fp8 one (which waits for two stages per iteration)."""
+    the next call on the same context is correct.  The 16-bit consumer, the
+    fp8 one (which waits for two stages per iteration), and both tcgen05
+    kernels (32 and 128 columns), whose MMA thread gives up on the missing
+    stage and frees its tensor memory."""
     import time
     if kind == "e4m3" and not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("torch without float8_e4m3fn")
-    B, Hq, Hkv, D, T = 1, 8, 8, 128, 300
-    q = fd_inputs.randn((B, Hq, D), "f16", 1201, device=DEV)
+    G, ql = {"f16_g8_q4": (8, 4), "bf16_g16_q8": (16, 8)}.get(kind, (1, 1))
+    dt = "bf16" if kind.startswith("bf16") else "f16"
+    B, Hkv, D, T = 1, 8 if G == 1 else 2, 128, 300
+    Hq = Hkv * G
+    q = fd_inputs.randn((B, ql, Hq, D) if ql > 1 else (B, Hq, D), dt, 1201, device=DEV)
     sc = {}
     if kind == "e4m3":
         k = fd_inputs.randn_fp8((B, Hkv, T, D), 1203, device=DEV, gain=16.0)
         v = fd_inputs.randn_fp8((B, Hkv, T, D), 1204, device=DEV, gain=16.0)
         sc = dict(k_scale=1 / 16, v_scale=1 / 16)
     else:
-        k, v = _cache(B, Hkv, T, D, "f16", 1202)
+        k, v = _cache(B, Hkv, T, D, dt, 1202)
     sl_h = np.array([T], dtype=np.int32)
     seqlens = torch.from_numpy(sl_h).to(DEV)
     desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=1, **sc)
     desc.flags = fd.FD_FLAG_TEST_DROP_FIRST_STAGE
     ws = torch.empty(fd.fd_workspace_size(desc, 1), dtype=torch.uint8, device=DEV)
-    out = torch.zeros(B, Hq, D, dtype=torch.float32, device=DEV)
+    out = torch.zeros(B, ql, Hq, D, dtype=torch.float32, device=DEV)
     assert fd.fd_device_status(clear=True) == fd.FD_OK
     t0 = time.time()
     fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, None, ws))
@@ -481,7 +486,7 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     assert time.time() - t0 < 60
     assert fd.fd_device_status(clear=True) == fd.FD_OK
     got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1, **sc)
-    ref_o, ref_l = oracle_all(q, k, v, sl_h, "f16", Hkv, kv_dtype=kind if kind == "e4m3" else None,
+    ref_o, ref_l = oracle_all(q, k, v, sl_h, dt, Hkv, kv_dtype=kind if kind == "e4m3" else None,
                               **sc)
     assert_parity(got_o, got_l, ref_o, ref_l, f"after a timed-out call ({kind})")
 
@@ -541,12 +546,15 @@ def test_query_blocks(q_len, group):
 def test_query_blocks_wide(group, q_len, dtype):
     """Query blocks of 72, 80 and 128 columns (one tcgen05 CTA serves a KV
     head's whole group) and of 144 and 256 columns (column blocks of 16),
-    against the oracle; one sequence shorter than the block."""
+    against the oracle; one sequence shorter than the block, and NaN in the
+    cache past its length."""
     B, Hkv, D, T = 2, 2, 128, 900
     Hq = Hkv * group
     q = fd_inputs.randn((B, q_len, Hq, D), dtype, 1450 + 10 * q_len + group, device=DEV)
     k, v = _cache(B, Hkv, T, D, dtype, 1550 + group)
     sl = np.array([900, 11], dtype=np.int32)
+    k[1, :, 11:] = float("nan")
+    v[1, :, 11:] = float("nan")
     ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
     for S in (0, 1, 5):
         got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
