@@ -103,10 +103,10 @@ cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const S
 // CTAs per (split, KV head) for G * q_len columns.
 inline int column_blocks(int cols) { return cols <= 8 ? 1 : (cols + 15) / 16; }
 
-// Query blocks wider than 16 columns (16-bit caches, tensor-core path) run
-// the tcgen05 variant: one CTA serves all columns (up to 128) and takes a
-// whole SM, so it is one work item per split and the planner counts one
-// slot per SM.
+// Query blocks of 17-128 columns (16-bit caches, tensor-core path) run a
+// tcgen05 variant (17-64 columns: the hi and lo parts of P stacked in M;
+// 65-128: one lane per column): one CTA serves all columns and takes a whole
+// SM, so it is one work item per split and the planner counts one slot per SM.
 inline bool use_umma(bool fp8, bool cuda_cores, int cols) {
     return !fp8 && !cuda_cores && cols > 16 && cols <= 128;
 }

@@ -1190,11 +1190,11 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 variant (KIND 31) for query blocks wider than 16 columns (16-bit
-// caches): one CTA serves all G * q_len (position, head) columns of a KV head,
-// up to 128, as the M rows of 5th-generation tensor-core MMAs with the
-// accumulators in tensor memory, instead of one CTA per 16 columns each
-// repeating the split's arithmetic on warp MMAs.
+// tcgen05 variant (KIND 31) for query blocks of 65-128 columns (16-bit
+// caches; KIND 32 below takes 17-64): one CTA serves all G * q_len
+// (position, head) columns of a KV head as the M rows of 5th-generation
+// tensor-core MMAs with the accumulators in tensor memory, instead of one CTA
+// per 16 columns each repeating the split's arithmetic on warp MMAs.
 //   S[col][tok]  = Q[col][:] . K[tok][:]        M = 128 columns, N = 64 tokens, K = 128 dims
 //   O[col][dim] += P[col][tok] . V[tok][dim]    M = 128, N = 128 dims, K = 64 tokens (V read MN-major)
 // Q (K-major, 128-byte swizzle) is staged once in shared memory; K and V come
