@@ -12,7 +12,7 @@ import torch
 import fd_inputs
 import oracle
 import split_kv_gb300 as fd
-from gpu_util import assert_parity, oracle_all, oracle_rows_contiguous, run_decode
+from gpu_util import assert_parity, oracle_all, oracle_rows_contiguous, planned_splits, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -398,6 +398,28 @@ def test_paged_b8_full_sampled_rows():
     rows = np.random.default_rng(5).choice(B * Hq, size=64, replace=False)
     ref_o, ref_l = oracle_all(q, pk, pv, sl, c["dtype"], Hkv, page_size=ps, block_table=bt, rows=rows)
     assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"paged_b8 S={S}")
+
+
+@pytest.mark.parametrize("name", ["query_block_q4", "query_block_g8_q4", "query_block_g8_q8",
+                                  "query_block_g16_q8"])
+def test_query_block_workloads_full_sampled_rows(name):
+    """The query-block workloads at full size (B = 4, 32K tokens) in the
+    bench's launch configuration (planned split count; warp MMAs at 16
+    columns, the tcgen05 kernels at 32, 64 and 128), sampled rows against the
+    oracle, every position of the block represented."""
+    c = fd_inputs.WORKLOADS[name]
+    B, Hq, Hkv, D, T, ql = (c["batch"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["ctx"],
+                            c["q_len"])
+    q = fd_inputs.randn((B, ql, Hq, D), c["dtype"], c["seed"], device=DEV)
+    k, v = _cache(B, Hkv, T, D, c["dtype"], c["seed"] + 10)
+    sl = np.full(B, T, dtype=np.int32)
+    got_o, got_l, S = run_decode(q, k, v, sl)
+    assert S == planned_splits(B, Hq, Hkv, ql, sl)
+    rng = np.random.default_rng(31)
+    rows = np.sort(np.concatenate([
+        ((b * ql + i) * Hq + rng.integers(0, Hq, size=1)) for b in range(B) for i in range(ql)]).ravel())
+    ref_o, ref_l = oracle_all(q, k, v, sl, c["dtype"], Hkv, rows=rows)
+    assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"{name} S={S}")
 
 
 @pytest.mark.parametrize("batch", [1, 4, 16, 64])
