@@ -51,9 +51,34 @@ def _case(i):
                 S=S, out_dtype=out_dtype, cuda_cores=cuda_cores, seed=6000 + 10 * i)
 
 
-@pytest.mark.parametrize("i", range(N_CASES))
-def test_random_problem(i):
-    c = _case(i)
+N_WIDE = 32
+
+
+def _wide_case(i):
+    """A query block of 17-256 columns per KV head: the tcgen05 kernels
+    (17-64, 65-128 on a 16-bit cache) and column blocks (fp8, or more than
+    128 columns); a third of the cases in each column range."""
+    rng = np.random.default_rng(7000 + i)
+    c = _case(10_000 + i)
+    lo, hi = [(17, 64), (65, 128), (129, 256)][i % 3]
+    while True:
+        G = int(rng.choice([3, 4, 5, 6, 8, 12, 16]))
+        ql = int(rng.choice([2, 3, 4, 5, 8, 12, 16]))
+        if lo <= G * ql <= hi:
+            break
+    if rng.random() < 0.8:                               # mostly 16-bit caches
+        c["kv"] = c["qd"] = str(rng.choice(["f16", "bf16"]))
+    T = int(rng.integers(1, 2500))
+    B = int(rng.integers(1, 4))
+    lens = rng.integers(0, T + 1, size=B)
+    lens[rng.integers(0, B)] = T
+    c.update(G=G, ql=ql, Hkv=int(rng.integers(1, 3)), B=B, T=T, lens=lens.astype(np.int32),
+             cuda_cores=False, seed=8000 + 10 * i)
+    return c
+
+
+def _run_case(c, what_prefix):
+    B, G, ql, Hkv, T, ps, D = c["B"], c["G"], c["ql"], c["Hkv"], c["T"], c["ps"], 128
     B, G, ql, Hkv, T, ps, D = c["B"], c["G"], c["ql"], c["Hkv"], c["T"], c["ps"], 128
     Hq = G * Hkv
     seed = c["seed"]
@@ -84,6 +109,16 @@ def test_random_problem(i):
     if c["out_dtype"] != torch.float32:
         # the output is rounded to 16 bits: compare with the rounded reference
         ref_o = torch.from_numpy(ref_o).to(c["out_dtype"]).double().numpy()
-    what = (f"case {i}: kv={c['kv']} q={c['qd']} G={G} q_len={ql} Hkv={Hkv} B={B} page={ps} "
+    what = (f"{what_prefix}: kv={c['kv']} q={c['qd']} G={G} q_len={ql} Hkv={Hkv} B={B} page={ps} "
             f"T={T} lens={c['lens'].tolist()} S={S} out={c['out_dtype']} cuda_cores={c['cuda_cores']}")
     assert_parity(got_o, got_l, ref_o, ref_l, what)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_problem(i):
+    _run_case(_case(i), f"case {i}")
+
+
+@pytest.mark.parametrize("i", range(N_WIDE))
+def test_random_wide_query_block(i):
+    _run_case(_wide_case(i), f"wide case {i}")

@@ -583,6 +583,24 @@ def test_query_blocks_wide(group, q_len, dtype):
         assert_parity(got_o, got_l, ref_o, ref_l, f"q_len={q_len} G={group} S={S}")
 
 
+@pytest.mark.parametrize("group,q_len", [(8, 4), (16, 8)])
+def test_query_blocks_wide_large_scores(group, q_len):
+    """Scores into the hundreds on the tcgen05 kernels (32 and 128 columns):
+    the lazily moved running max (moved only when a stage's max exceeds it by
+    more than 2^8) must keep every weight finite and the merge exact."""
+    B, Hkv, D, T = 2, 2, 128, 4096
+    Hq = Hkv * group
+    k, v = _cache(B, Hkv, T, D, "bf16", 1650 + group)
+    sl = np.array([4096, 700], dtype=np.int32)
+    for gain in (18.0, 40.0):
+        q = fd_inputs.randn((B, q_len, Hq, D), "bf16", 1660 + group, device=DEV, gain=gain)
+        ref_o, ref_l = oracle_all(q, k, v, sl, "bf16", Hkv)
+        for S in (0, 1, 6):
+            got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+            assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} q_len={q_len} gain={gain} S={S}")
+            assert np.all(np.isfinite(got_l))
+
+
 def test_query_block_wide_paged():
     """A paged 128-column block (G = 16, q_len = 8) on the tcgen05 path."""
     B, Hkv, G, D, ps, ql = 2, 2, 16, 128, 64, 8
