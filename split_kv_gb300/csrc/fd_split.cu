@@ -1240,7 +1240,6 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     // mbarriers, each [2] by stage parity except drain and the pairs'
     const uint32_t b_pair0 = smem_u32(xsum + 256);   // [4], one per lane quarter: one arrival per warp of the pair
     const uint32_t b_s_full = b_pair0 + 32;   // one arrival (MMA commit): S written
-    const uint32_t b_s_free = b_pair0 + 48;   // one arrival per softmax warp: S read
     const uint32_t b_p_full = b_pair0 + 64;   // one arrival per softmax warp: P written (and O rescaled)
     const uint32_t b_o_done = b_pair0 + 80;   // one arrival (MMA commit): PV done
     const uint32_t b_drain = b_pair0 + 96;    // one arrival (MMA commit): every MMA done
@@ -1251,7 +1250,6 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_s_full + 8u * b, 1);
-            mbar_init(b_s_free + 8u * b, Gm::kWarps);
             mbar_init(b_p_full + 8u * b, Gm::kWarps);
             mbar_init(b_o_done + 8u * b, 1);
         }
@@ -1288,6 +1286,12 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     if (warp == Gm::kWarps + 1) {
         // ---- MMA issue: S of stage i + 1 goes out before PV of stage i, so
         // the softmax of one stage overlaps the tensor cores' work on the next
+        // Buffer reuse needs no waits of its own: S of stage i + 1 overwrites
+        // the scores of stage i - 1, which the softmax read before it handed
+        // over P of stage i - 1 (waited for before PV of stage i - 1); and the
+        // commit that signals S of stage i completes only after every earlier
+        // MMA, PV of stage i - 2 included, so the softmax may then overwrite
+        // that stage's P buffer.
         if (lane == 0) {
             // Issue cost bounds this thread: each descriptor is built once and
             // offset by constants (the start address is the low field, in
@@ -1321,7 +1325,6 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                 if (i + 1 < n_sub) {
                     const int j = i + 1;
                     ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
-                    if (ok && j >= 2) ok = wait_or_flag(b_s_free + 8u * (j & 1), ((j >> 1) - 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j);
@@ -1381,9 +1384,6 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     for (int e = 0; e < 16; ++e) t[16 * q + e] = __uint_as_float(v[e]) * sc;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_s_free + 8u * buf);
             const int tok = c.tok0 + i * Gm::kSub;
             const int nvalid = min(Gm::kSub, c.tok1 - tok);
             const bool partial = nvalid < Gm::kSub;
@@ -1426,11 +1426,6 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     hi[e] = Mma<T>::pack(p0, p1, k0, k1);
                     lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
                 }
-            }
-            if (i >= 2) {   // PV of stage i - 2 has read this P buffer
-                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * buf, ((i >> 1) - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
             }
             if (quarter_active) {
                 // this warp's 32 tokens: hi in its first 16 columns, lo in the next 16
@@ -1580,7 +1575,6 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
     // mbarriers, [2] by stage parity unless noted
     const uint32_t b_grp0 = smem_u32(xsum + 256);   // [2], one per column group: one arrival per warp of its four
     const uint32_t b_s_full = b_grp0 + 16;    // one arrival (MMA commit): S written
-    const uint32_t b_s_free = b_grp0 + 32;    // one arrival per softmax warp: S read
     const uint32_t b_p_full = b_grp0 + 48;    // one arrival per softmax warp: P written (and O rescaled)
     const uint32_t b_o_done = b_grp0 + 64;    // one arrival (MMA commit): PV done
     const uint32_t b_drain = b_grp0 + 80;     // single, one arrival (MMA commit): every MMA done
@@ -1590,7 +1584,6 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_grp0 + 8u * b, 4);
             mbar_init(b_s_full + 8u * b, 1);
-            mbar_init(b_s_free + 8u * b, Gm::kWarps);
             mbar_init(b_p_full + 8u * b, Gm::kWarps);
             mbar_init(b_o_done + 8u * b, 1);
         }
@@ -1627,6 +1620,12 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
         // ---- MMA issue (one thread): S of stage i + 1 goes out before PV of stage i.
         // Each descriptor is built once and offset by constants (the start address
         // is the low field, in 16-byte units, and no operand crosses 256 KB).
+        // Buffer reuse needs no waits of its own: S of stage i + 1 overwrites
+        // the scores of stage i - 1, which the softmax read before it handed
+        // over P of stage i - 1 (waited for before PV of stage i - 1); and the
+        // commit that signals S of stage i completes only after every earlier
+        // MMA, PV of stage i - 2 included, so the softmax may then overwrite
+        // that stage's P buffer.
         if (lane == 0) {
             const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
             const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
@@ -1658,7 +1657,6 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
                 if (i + 1 < n_sub) {
                     const int j = i + 1;
                     ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
-                    if (ok && j >= 2) ok = wait_or_flag(b_s_free + 8u * (j & 1), ((j >> 1) - 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j);
@@ -1714,9 +1712,6 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(v[e]) * sc;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_s_free + 8u * buf);
             const int tok = c.tok0 + i * Gm::kSub;
             const int nvalid = min(Gm::kSub, c.tok1 - tok);
             const bool partial = nvalid < Gm::kSub;
@@ -1759,10 +1754,6 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
                     hi[e] = Mma<T>::pack(p0, p1, k0, k1);
                     lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
                 }
-            }
-            if (i >= 2) {   // PV of stage i - 2 has read this P buffer
-                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * buf, ((i >> 1) - 1) & 1));
-                if (!ok) break;
             }
             if (group_active) {
                 // tokens 16 tq .. +15 = chunks 2 tq, 2 tq + 1 of rows col (hi) and 64 + col (lo)
