@@ -1363,6 +1363,8 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
         const bool quarter_active = quarter * 32 < p.cols;   // the pair's columns hold queries
         const bool real = r < p.cols;
         const int vis = real ? c.L - p.q_len + 1 + r / p.group : c.L;
+        // scores stay raw until the exponent: sc (log2(e) / sqrt(d), a 16-bit
+        // cache) is positive, so maxima of raw scores scale to maxima of scaled ones
         const float sc = p.score_scale_log2;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t b_pair = b_pair0 + 8u * quarter;   // warps quarter and quarter + 4
@@ -1381,7 +1383,7 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                     tmem_ld16(tmem + lane_base + 64u * buf + 32u * h + 16u * q, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) t[16 * q + e] = __uint_as_float(v[e]) * sc;
+                    for (int e = 0; e < 16; ++e) t[16 * q + e] = __uint_as_float(v[e]);
                 }
             }
             const int tok = c.tok0 + i * Gm::kSub;
@@ -1409,7 +1411,7 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                 if (lane == 0) mbar_arrive(b_pair);
                 ok = __all_sync(kFull, wait_or_flag(b_pair, i & 1));
                 if (!ok) break;
-                mx = fmaxf(mx, xm[(h ^ 1) * 128 + r]);
+                mx = fmaxf(mx, xm[(h ^ 1) * 128 + r]) * sc;   // raw scores: sc > 0 keeps the max
                 need = mx > m_run + 8.f;       // also true for the first finite max
                 if (need) {
                     alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
@@ -1419,8 +1421,8 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
                 const float mu = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(t[2 * e] - mu);
-                    const float p1 = fast_exp2(t[2 * e + 1] - mu);
+                    const float p0 = fast_exp2(fmaf(t[2 * e], sc, -mu));
+                    const float p1 = fast_exp2(fmaf(t[2 * e + 1], sc, -mu));
                     l_run += p0 + p1;
                     float k0, k1, d0, d1;
                     hi[e] = Mma<T>::pack(p0, p1, k0, k1);
@@ -1694,6 +1696,8 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
         const bool group_active = 32 * g < p.cols;
         const bool real = col < p.cols;
         const int vis = real ? c.L - p.q_len + 1 + col / p.group : c.L;
+        // scores stay raw until the exponent: sc (log2(e) / sqrt(d), a 16-bit
+        // cache) is positive, so maxima of raw scores scale to maxima of scaled ones
         const float sc = p.score_scale_log2;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t b_grp = b_grp0 + 8u * g;
@@ -1710,7 +1714,7 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
                 tmem_ld16(tmem + lane_base + 64u * buf + 16u * tq, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(v[e]) * sc;
+                for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(v[e]);
             }
             const int tok = c.tok0 + i * Gm::kSub;
             const int nvalid = min(Gm::kSub, c.tok1 - tok);
@@ -1737,7 +1741,7 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
                 if (lane == 0) mbar_arrive(b_grp);
                 ok = __all_sync(kFull, wait_or_flag(b_grp, i & 1));
                 if (!ok) break;
-                mx = fmaxf(fmaxf(xm[col], xm[64 + col]), fmaxf(xm[128 + col], xm[192 + col]));
+                mx = fmaxf(fmaxf(xm[col], xm[64 + col]), fmaxf(xm[128 + col], xm[192 + col])) * sc;
                 need = mx > m_run + 8.f;       // also true for the first finite max
                 if (need) {
                     alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
@@ -1747,8 +1751,8 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
                 const float mu = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float p0 = fast_exp2(t[2 * e] - mu);
-                    const float p1 = fast_exp2(t[2 * e + 1] - mu);
+                    const float p0 = fast_exp2(fmaf(t[2 * e], sc, -mu));
+                    const float p1 = fast_exp2(fmaf(t[2 * e + 1], sc, -mu));
                     l_run += p0 + p1;
                     float k0, k1, d0, d1;
                     hi[e] = Mma<T>::pack(p0, p1, k0, k1);
