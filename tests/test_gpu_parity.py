@@ -202,6 +202,26 @@ def test_paged_identity_table_is_bitwise_contiguous(ps):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+@pytest.mark.parametrize("group,q_len", [(8, 4), (16, 8)])
+def test_tcgen05_bitwise_repeatable_and_paged_identity(group, q_len):
+    """The tcgen05 kernels (32 and 128 columns): two runs agree bit for bit,
+    and a pool holding the contiguous cache page by page, read through the
+    identity table, gives the contiguous result bit for bit."""
+    B, Hkv, D, T, ps = 2, 2, 128, 4096, 64
+    k, v = _cache(B, Hkv, T, D, "bf16", 811)
+    q = fd_inputs.randn((B, q_len, Hkv * group, D), "bf16", 812, device=DEV)
+    npp = T // ps
+    pk = k.reshape(B, Hkv, npp, ps, D).permute(0, 2, 1, 3, 4).reshape(B * npp, Hkv, ps, D).contiguous()
+    pv = v.reshape(B, Hkv, npp, ps, D).permute(0, 2, 1, 3, 4).reshape(B * npp, Hkv, ps, D).contiguous()
+    bt = np.arange(B * npp, dtype=np.int32).reshape(B, npp)
+    sl = np.array([4096, 2500], dtype=np.int32)
+    o1, l1, _ = run_decode(q, k, v, sl, n_splits=6)
+    o2, l2, _ = run_decode(q, k, v, sl, n_splits=6)
+    o3, l3, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=6)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
+
+
 # ---------------------------------------------------------------- determinism, halves
 def test_bitwise_repeatable_and_halves_equal_whole():
     B, Hq, Hkv, D, T = 2, 32, 8, 128, 6000
@@ -225,7 +245,7 @@ def test_bitwise_repeatable_and_halves_equal_whole():
     assert np.array_equal(lse.cpu().double().numpy().reshape(-1), l1)
 
 
-@pytest.mark.parametrize("kind", ["f16", "bf16_cuda_cores", "fp8_block"])
+@pytest.mark.parametrize("kind", ["f16", "bf16_cuda_cores", "fp8_block", "bf16_g8_q4", "f16_g16_q8"])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_one_split_writes_the_result_directly(kind, out_dtype):
     """With one split fd_decode (and fd_decode_static) skip the combine: the
@@ -243,6 +263,11 @@ def test_one_split_writes_the_result_directly(kind, out_dtype):
         v = fd_inputs.randn_fp8((B, Hkv, T, D), 1952, device=DEV, gain=16.0)
         q = fd_inputs.randn((B, ql, Hkv * G, D), "bf16", 1953, device=DEV)
         sc = dict(k_scale=1 / 16, v_scale=1 / 16)
+    elif kind in ("bf16_g8_q4", "f16_g16_q8"):   # the two tcgen05 kernels
+        G, ql = (8, 4) if kind == "bf16_g8_q4" else (16, 8)
+        dt = kind.split("_")[0]
+        k, v = _cache(B, Hkv, T, D, dt, 1956)
+        q = fd_inputs.randn((B, ql, Hkv * G, D), dt, 1957, device=DEV)
     else:
         G, ql = 4, 1
         dt = "f16" if kind == "f16" else "bf16"
