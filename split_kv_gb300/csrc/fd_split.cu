@@ -25,6 +25,10 @@
 //    consume_tc (default) runs QK^T and PV as warp MMAs fed by ldmatrix;
 //    consume_f8 builds the same MMAs' fragments from e4m3 bytes in registers;
 //    consume_simt (FD_FLAG_CUDA_CORES) uses FP32 FMAs, a half-warp per K row.
+//  - Query blocks of 17-128 columns on a 16-bit cache run instead on 5th-
+//    generation tensor cores (fd_split_umma64_kernel, fd_split_umma_kernel):
+//    one CTA per split holds every column as the M rows of tcgen05 MMAs with
+//    S and O accumulated in tensor memory, fed by the same TMA stages.
 //  - Scores are kept in base 2: t = (q.k) * log2(e)/sqrt(D), p = 2^(t - m).
 //    The workspace m is converted back to natural units of s.
 //  - Every mbarrier wait is bounded (2 s of wall time); on timeout the kernel
