@@ -123,10 +123,113 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
     if (p.lse != nullptr && t == 0) p.lse[row] = empty ? -INFINITY : M + logf(L);
 }
 
+// Many rows (query blocks): one warp per row, four rows per CTA, so thousands
+// of rows fit in one wave instead of queueing CTAs of four warps.  Lane l
+// holds dims 4l .. 4l + 3 and the m, l of splits l, l + 32, ...; the partial
+// outputs are requested kPre splits at a time and added in split order.
+constexpr int kRowsPerCta = 4;
+
+__global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const CombineParams p) {
+    grid_dependency_trigger();
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+    if (row >= p.rows) return;
+    const int S = p.n_splits;
+    const int64_t base = static_cast<int64_t>(row) * S;
+    const float4* urow = reinterpret_cast<const float4*>(p.ws_u + base * kHeadDim) + lane;
+    constexpr int kStride = kHeadDim / 4;   // float4s per split
+    float4 pre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) pre[k] = k < S ? urow[k * kStride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mv[kMaxSplits / 32], lv[kMaxSplits / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxSplits / 32; ++j) {
+        const int i = lane + 32 * j;
+        mv[j] = i < S ? p.ws_m[base + i] : -INFINITY;
+        lv[j] = i < S ? p.ws_l[base + i] : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxSplits / 32; ++j) M = fmaxf(M, mv[j]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+    float L = 0.f, wv[kMaxSplits / 32];
+#pragma unroll
+    for (int j = 0; j < kMaxSplits / 32; ++j) {
+        wv[j] = (mv[j] == -INFINITY || M == -INFINITY) ? 0.f : fast_exp2((mv[j] - M) * kLog2e);
+        L = fmaf(wv[j], lv[j], L);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
+    // the weight of split i, held by lane i % 32 in wv[i / 32]
+    auto weight = [&](int i) {
+        const int j = i >> 5;
+        const float x = j == 0 ? wv[0] : j == 1 ? wv[1] : j == 2 ? wv[2] : wv[3];
+        return __shfl_sync(kFullMask, x, i & 31);
+    };
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const float wt = weight(k);
+        if (k < S) {
+            a.x = fmaf(wt, pre[k].x, a.x);
+            a.y = fmaf(wt, pre[k].y, a.y);
+            a.z = fmaf(wt, pre[k].z, a.z);
+            a.w = fmaf(wt, pre[k].w, a.w);
+        }
+    }
+    for (int i0 = kPre; i0 < S; i0 += kPre) {
+        float4 u[kPre];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k)
+            u[k] = i0 + k < S ? urow[(i0 + k) * kStride] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const float wt = weight(i0 + k);
+            if (i0 + k < S) {
+                a.x = fmaf(wt, u[k].x, a.x);
+                a.y = fmaf(wt, u[k].y, a.y);
+                a.z = fmaf(wt, u[k].z, a.z);
+                a.w = fmaf(wt, u[k].w, a.w);
+            }
+        }
+    }
+    const bool empty = (M == -INFINITY) || !(L > 0.f);
+    const float4 o = empty ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(a.x / L, a.y / L, a.z / L, a.w / L);
+    const int64_t oi = static_cast<int64_t>(row) * kHeadDim + 4 * lane;
+    if (p.out_dtype == 2) {   // out carries only its element alignment: scalar stores
+        float* d = static_cast<float*>(p.out) + oi;
+        d[0] = o.x;
+        d[1] = o.y;
+        d[2] = o.z;
+        d[3] = o.w;
+    } else if (p.out_dtype == 0) {
+        __half* d = static_cast<__half*>(p.out) + oi;
+        d[0] = __float2half_rn(o.x);
+        d[1] = __float2half_rn(o.y);
+        d[2] = __float2half_rn(o.z);
+        d[3] = __float2half_rn(o.w);
+    } else {
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + oi;
+        d[0] = __float2bfloat16_rn(o.x);
+        d[1] = __float2bfloat16_rn(o.y);
+        d[2] = __float2bfloat16_rn(o.z);
+        d[3] = __float2bfloat16_rn(o.w);
+    }
+    if (p.lse != nullptr && lane == 0) p.lse[row] = empty ? -INFINITY : M + logf(L);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
     if (p.rows <= 0) return cudaSuccess;
+    // a CTA of four warps per row shortens each row's chain when rows are few
+    // (a decode step's query heads); with a thousand rows or more, a warp per
+    // row keeps the launch to one wave
+    if (p.rows >= 1024)
+        return launch_pdl(fd_combine_rows_kernel, dim3((p.rows + kRowsPerCta - 1) / kRowsPerCta),
+                          dim3(32 * kRowsPerCta), 0, stream, p);
     return launch_pdl(fd_combine_kernel, dim3(p.rows), dim3(kHeadDim), 0, stream, p);
 }
 

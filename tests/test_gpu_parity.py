@@ -626,6 +626,25 @@ def test_query_blocks_wide_large_scores(group, q_len):
             assert np.all(np.isfinite(got_l))
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_combine_of_many_rows(out_dtype):
+    """1024 query rows (a warp of the combine per row): 3 and 40 splits (past
+    the first 32 a lane holds), an empty sequence and a short one, every
+    output dtype, against the oracle."""
+    B, Hkv, G, ql, D, T = 8, 2, 16, 4, 128, 700
+    Hq = Hkv * G
+    q = fd_inputs.randn((B, ql, Hq, D), "bf16", 1680, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "bf16", 1681)
+    sl = np.array([700, 0, 5, 350, 699, 64, 1, 700], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, "bf16", Hkv)
+    if out_dtype != torch.float32:
+        ref_o = torch.from_numpy(ref_o).to(out_dtype).double().numpy()
+    for S in (3, 40):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S, out_dtype=out_dtype)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"1024 rows S={S} out={out_dtype}")
+        assert np.all(got_o.reshape(B, -1)[1] == 0.0) and np.all(np.isneginf(got_l.reshape(B, -1)[1]))
+
+
 def test_query_block_wide_paged():
     """A paged 128-column block (G = 16, q_len = 8) on the tcgen05 path."""
     B, Hkv, G, D, ps, ql = 2, 2, 16, 128, 64, 8
