@@ -1260,6 +1260,11 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
         mbar_init(b_drain, 1);
         fence_barrier_init();
     }
+    __syncthreads();   // every barrier is initialised
+    if (warp == Gm::kWarps) {   // the producer streams at once; Q and tensor memory follow
+        produce<31>(c, &tmK, &tmV, lane);
+        return;
+    }
     if (threadIdx.x < 128) {
         // Q tile: row r is column r of the group (zeros past the columns)
         const int r = threadIdx.x;
@@ -1275,16 +1280,12 @@ __global__ void __launch_bounds__(Geo<31>::kThreads, 1)
     }
     if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    named_sync(3, kSoftmaxThreads + 32);   // the softmax warps and the MMA warp
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_p = tmem + 128;
     const uint32_t tmem_o = tmem + 256;
 
-    if (warp == Gm::kWarps) {
-        produce<31>(c, &tmK, &tmV, lane);
-        return;
-    }
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
 
     if (warp == Gm::kWarps + 1) {
@@ -1596,6 +1597,11 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
         mbar_init(b_drain, 1);
         fence_barrier_init();
     }
+    __syncthreads();   // every barrier is initialised
+    if (warp == Gm::kWarps) {   // the producer streams at once; Q and tensor memory follow
+        produce<32>(c, &tmK, &tmV, lane);
+        return;
+    }
     if (threadIdx.x < 128) {
         // Q tile: rows r and 64 + r are column r of the group (zeros past the columns)
         const int r = threadIdx.x;
@@ -1611,15 +1617,11 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
     }
     if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    named_sync(3, kSoftmaxThreads + 32);   // the softmax warps and the MMA warp
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_o = tmem + 128;
 
-    if (warp == Gm::kWarps) {
-        produce<32>(c, &tmK, &tmV, lane);
-        return;
-    }
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
 
     if (warp == Gm::kWarps + 1) {
