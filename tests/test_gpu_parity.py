@@ -669,6 +669,21 @@ def test_query_block_paged_and_strided():
     assert_parity(got_o, got_l, ref_o, ref_l, "paged query block")
 
 
+@pytest.mark.parametrize("group,dtype", [(24, "f16"), (32, "bf16"), (64, "f16"), (128, "bf16")])
+def test_large_groups_single_query(group, dtype):
+    """One query per sequence with 24 to 128 query heads per KV head (MQA-like
+    groups): the group's heads are the tcgen05 kernels' columns."""
+    B, Hkv, D, T = 2, 1, 128, 1800
+    Hq = Hkv * group
+    q = fd_inputs.randn((B, Hq, D), dtype, 1720 + group, device=DEV)
+    k, v = _cache(B, Hkv, T, D, dtype, 1730 + group)
+    sl = np.array([1800, 37], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl, dtype, Hkv)
+    for S in (0, 1, 4):
+        got_o, got_l, _ = run_decode(q, k, v, sl, n_splits=S)
+        assert_parity(got_o, got_l, ref_o, ref_l, f"G={group} S={S}")
+
+
 @pytest.mark.parametrize("group", [3, 5, 16])
 def test_other_group_sizes_single_query(group):
     """Groups that are not powers of two, and a 16-wide group, on the
