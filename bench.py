@@ -16,6 +16,13 @@ Printed (one JSON line on rank 0):
                fd_decode, out/lse copied back
   cpu_baseline the fp64 oracle on the host cores on a bounded sample
   clocks       SM clocks and throttle reasons sampled during the timed region
+  step_ms      mean / median / min / max of the per-step CUDA-event times
+  configs      every configuration of the workloads (tiny MHA with forced
+               split counts, the ragged batch, the paged cache, sweep points
+               with n_splits = 1 beside the plan, the fp8 cache, the query
+               blocks): us per call, K+V GB/s, fraction of the measured HBM
+               peak, split and combine kernel times, and the oracle timed on
+               sampled rows of the same problem
 
 --impl reference times the oracle (the only reference this method has) on
 the same workload, a bounded sample per step.
@@ -53,6 +60,8 @@ def _args():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline only (no per-configuration measurements)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every call from Python instead of replaying a captured CUDA graph")
     ap.add_argument("--cuda-cores", action="store_true",
@@ -76,34 +85,102 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    """SM clocks and clock-event (throttle) reasons of the benchmarked GPU,
+    sampled in the background: through NVML every 2 ms when libnvidia-ml can
+    be loaded, else with nvidia-smi every 50 ms.  The GPU is addressed by its
+    UUID, so the samples are of the device CUDA runs on.  mark() brackets the
+    timed region; stop() summarises the samples inside it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+    def __init__(self, dev_index: int):
+        import torch
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        self.uuid = u if u.startswith("GPU-") else "GPU-" + u
+        self.idx = dev_index
+        self.samples = []          # (host time, sm MHz, reasons bitmask or names)
+        self.window = None
+        self.max_mhz = None
+        self.source = None
+        self._stop = False
+        self._thread = None
         self.proc = None
-        # the raw samples go to $FD_BENCH_LOG_DIR (default: the temp directory)
+        # the raw nvidia-smi samples go to $FD_BENCH_LOG_DIR (default: the temp directory)
         log_dir = os.environ.get("FD_BENCH_LOG_DIR") or tempfile.gettempdir()
         self.path = os.path.join(log_dir, f"clocks_bench_{os.getpid()}.csv")
 
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, h, reasons
+
     def start(self):
+        import threading
+        try:
+            lib, h, reasons = self._nvml()
+            import ctypes
+
+            def loop():
+                clk, r = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop:
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                            reasons(h, ctypes.byref(r)) == 0:
+                        self.samples.append((time.perf_counter(), float(clk.value), int(r.value)))
+                    time.sleep(0.002)
+
+            self.source = "nvml, 2 ms"
+            self._thread = threading.Thread(target=loop, daemon=True)
+            self._thread.start()
+            return
+        except Exception:
+            pass
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi, 50 ms"
             t0 = time.time()
             while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
                 time.sleep(0.05)
         except Exception:
             self.proc = None
 
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
+
     def stop(self):
+        if self._thread is not None:
+            time.sleep(0.01)
+            self._stop = True
+            self._thread.join(timeout=5)
+            rows = self.samples
+            inside = [x for x in rows if self.window and self.window[0] <= x[0] <= self.window[1]]
+            use = inside or rows
+            if not use:
+                return None
+            names = sorted({n for x in use for b, n in self.REASON_BITS.items() if x[2] & b})
+            return {"sm_mhz": statistics.median(x[1] for x in use),
+                    "sm_max_mhz": self.max_mhz or max(x[1] for x in use), "reasons": names,
+                    "samples": len(rows), "samples_in_timed_region": len(inside),
+                    "sm_mhz_min": min(x[1] for x in use), "source": self.source}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -126,7 +203,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i, s in enumerate(r[2]) if s.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": self.source}
 
 
 def _dist():
@@ -333,15 +410,21 @@ def run_gpu(args):
         sampler.start()
     _barrier(ws)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    # an event between consecutive steps: one pair per step, and the whole region
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_host0 = time.perf_counter()
+    evs[0].record(stream)
+    for i in range(args.steps):
         run_step()
-    e1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
     _barrier(ws)
+    if sampler:
+        sampler.mark(t_host0, t_host1)
     clocks = sampler.stop() if sampler else None
-    ms_local = e0.elapsed_time(e1) / args.steps
+    ms_local = evs[0].elapsed_time(evs[-1]) / args.steps
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     fd.check(fd.fd_device_status(stream), "device status after timing")
 
     kv_bytes_layer = B * Hkv * T * D * 2 * 2
@@ -494,10 +577,19 @@ def run_gpu(args):
                "sample": f"one layer of the workload (all {B * Hq} query rows, {T} tokens) "
                          f"x {reps} repetitions, fp64; {t_layer * 1e6:.0f} us/layer"}
 
+    # ---- every configuration of the workloads, rank 0 at N=1 only (the
+    # replicas of N>1 run the headline alone)
+    configs = None
+    if rank == 0 and ws == 1 and not args.no_configs:
+        configs = measure_configs(dev, stream, peak, args.eager, with_cpu=not args.no_cpu_baseline)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": us_layer,
+            "step_ms": {"mean": statistics.mean(step_ms), "median": statistics.median(step_ms),
+                        "min": min(step_ms), "max": max(step_ms), "n": len(step_ms),
+                        "us_per_layer_median": statistics.median(step_ms) * 1e3 / n_layers},
             "frac_of_hbm_peak": value / peak, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic N(0,1), seeded, fp16 cache",
             "config": _config(c, S), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -505,6 +597,7 @@ def run_gpu(args):
             "workspace_bytes": wsb, "num_sms": fd.fd_num_sms(),
             "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores",
             "launch": graph_note,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -584,6 +677,7 @@ def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
     else:
         sl_h = np.full(B, T, dtype=np.int32)
     q_len = c.get("q_len", 1)
+    bt_h = None
     for j in range(n_sets):
         qshape = (B, q_len, Hq, D) if q_len > 1 else (B, Hq, D)
         q = fd_inputs.randn(qshape, dt, seed + 100 * j, device=dev)
@@ -593,7 +687,8 @@ def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
             n_pages = B * npp
             k = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), dt, seed + 100 * j + 1, device=dev)
             v = fd_inputs.randn_chunked((n_pages, Hkv, ps, D), dt, seed + 100 * j + 2, device=dev)
-            bt = torch.from_numpy(fd_inputs.block_table(seed + 2, B, npp, n_pages)).to(dev)
+            bt_h = fd_inputs.block_table(seed + 2, B, npp, n_pages)
+            bt = torch.from_numpy(bt_h).to(dev)
             desc = fd.make_desc(q, k, v, page_size=ps, max_pages_per_seq=npp, max_seqlen=int(sl_h.max()))
         elif c.get("kv_dtype") == "e4m3":
             gk = c["kv_gain"]
@@ -607,96 +702,194 @@ def _problem_sets(name, c, dev, n_sets, batch=None, ctx=None):
             bt = None
             desc = fd.make_desc(q, k, v, max_seqlen=int(sl_h.max()))
         sets.append((desc, q, k, v, bt))
-    return sets, sl_h
+    return sets, sl_h, bt_h
+
+
+def _oracle_sample(c, sets, sl_h, bt_h, kv_bytes, target_s):
+    """The fp64 oracle, as it stands, on a seeded sample of the problem's query
+    rows (set 0) on every host core, sized to about target_s seconds.  The
+    KV-read rate counts the fraction of the layer's (row, key) pairs the
+    sample covers."""
+    import numpy as np
+
+    import oracle
+    desc, q, k, v, _ = sets[0]
+    B, Hq, Hkv = desc.batch, c["n_q_heads"], c["n_kv_heads"]
+    ql = c.get("q_len", 1)
+    okw = dict(dtype=c["dtype"], n_kv_heads=Hkv, n_threads=oracle.hardware_threads())
+    if c.get("kv_dtype") == "e4m3":
+        okw.update(kv_dtype="e4m3", k_scale=desc.k_scale, v_scale=desc.v_scale)
+    if bt_h is not None:
+        okw.update(page_size=c["page_size"], block_table=bt_h)
+    qh, kh, vh = q.cpu(), k.cpu(), v.cpu()
+    # row (b*q_len + i)*Hq + h sees the first L_b - q_len + 1 + i keys
+    vis = np.array([max(0, int(sl_h[r // (ql * Hq)]) - ql + 1 + (r // Hq) % ql)
+                    for r in range(B * ql * Hq)], dtype=np.float64)
+    order = np.random.default_rng(7).permutation(B * ql * Hq)
+    threads = okw["n_threads"]
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.decode(qh, kh, vh, sl_h, rows=rows, **okw)
+        return time.perf_counter() - t0
+
+    n = min(threads, len(order))
+    t = run(np.sort(order[:n]))
+    n = int(max(n, min(len(order), n * target_s / max(t, 1e-6))))
+    rows = np.sort(order[:n])
+    t = run(rows)
+    frac = vis[rows].sum() / max(vis.sum(), 1.0)
+    return {"value": kv_bytes * frac / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "us_per_layer": t / max(frac, 1e-12) * 1e6,
+            "sample": f"{n} of the {len(order)} query rows of one layer (seeded), fp64, "
+                      f"{t:.2f} s; rate scaled by the sampled fraction of (row, key) pairs"}
+
+
+def measure_problem(name, c, dev, stream, peak, *, batch=None, ctx=None, forced=(), unsplit=False,
+                    eager=False, cuda_cores=False, warmup=3, cpu_seconds=0.0):
+    """Device time per fd_decode call of one workload problem (inputs rotated
+    across distinct sets larger than the L2, the calls replayed from a CUDA
+    graph), at the planned split count and at `forced` ones (and 1 if
+    `unsplit`); the split and combine kernels timed alone at the planned
+    count; optionally the oracle on sampled rows."""
+    import math as _m
+
+    import torch
+
+    import split_kv_gb300 as fd
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    B = batch or c["batch"]
+    T = ctx or c["ctx"]
+    fp8 = c.get("kv_dtype") == "e4m3"
+    esize = 1 if fp8 else 2
+    est = B * c["n_kv_heads"] * T * c["head_dim"] * esize * 2
+    n_sets = max(1, min(256, _m.ceil(4 * l2 / max(est, 1))))
+    sets, sl_h, bt_h = _problem_sets(name, c, dev, n_sets, batch, ctx)
+    seqlens = torch.from_numpy(sl_h).to(dev)
+    kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * esize * 2
+    ql = c.get("q_len", 1)
+    rows = B * ql * c["n_q_heads"]
+    d0 = sets[0][0].copy()
+    if cuda_cores:
+        d0.flags = fd.FD_FLAG_CUDA_CORES
+    S_plan = fd.check(fd.fd_plan_desc(d0, sl_h), "fd_plan_desc")
+    if ql == 1 and not fp8 and not cuda_cores:
+        assert S_plan == fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
+    counts = [S_plan] + [S for S in forced if S != S_plan]
+    if unsplit and S_plan != 1 and 1 not in counts:
+        counts.append(1)
+    iters = max(50, min(2000, int(1e10 / max(kv_bytes, 1))))
+    res = {"workload": name, "batch": B, "ctx": T, "q_len": ql, "n_q_heads": c["n_q_heads"],
+           "n_kv_heads": c["n_kv_heads"], "kv_dtype": c.get("kv_dtype", c["dtype"]),
+           "n_splits": S_plan, "kv_bytes": kv_bytes, "input_sets": n_sets, "peak_gbs": peak}
+    by_splits = {}
+    for S in counts:
+        descs = []
+        for (desc, *_rest) in sets:
+            d = desc.copy()
+            d.n_splits = S
+            if cuda_cores:
+                d.flags = fd.FD_FLAG_CUDA_CORES
+            descs.append(d)
+        wsb = fd.fd_workspace_size(descs[0], S)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        out = torch.empty(rows, c["head_dim"], dtype=torch.float32, device=dev)
+        lse = torch.empty(rows, dtype=torch.float32, device=dev)
+
+        def call(j, h):
+            _, q, k, v, bt = sets[j]
+            rc = fd.fd_decode(descs[j], q, k, v, seqlens, bt, out, lse, ws, wsb, stream=h)
+            if rc != 0:
+                raise fd.FdError(rc, "fd_decode")
+
+        ms, note = _time_calls(call, n_sets, iters, max(3, warmup), stream, dev, eager)
+        by_splits[S] = ms * 1e3
+        if S == S_plan:
+            res["launch"] = note
+            if S > 1:
+                def split(j, h):
+                    _, q, k, v, bt = sets[j]
+                    fd.check(fd.fd_split_states(descs[j], q, k, v, seqlens, bt, ws, wsb, stream=h))
+
+                def combine(j, h):
+                    fd.check(fd.fd_combine_states(descs[j], ws, out, lse, wsb, stream=h))
+
+                res["split_us"] = _time_calls(split, n_sets, iters, 2, stream, dev, eager)[0] * 1e3
+                res["combine_us"] = _time_calls(combine, n_sets, iters, 2, stream, dev, eager)[0] * 1e3
+            else:   # one split: the split kernel writes the result, no combine
+                res["split_us"], res["combine_us"] = ms * 1e3, 0.0
+        del ws
+    fd.check(fd.fd_device_status(stream), "device status")
+    us = by_splits[S_plan]
+    res["us_per_call"] = us
+    res["kv_gbs"] = kv_bytes / (us * 1e-6) / 1e9
+    res["frac_of_hbm_peak"] = res["kv_gbs"] / peak
+    if len(by_splits) > 1:
+        res["us_per_call_by_splits"] = {str(S): t for S, t in by_splits.items()}
+    if unsplit and 1 in by_splits:
+        res["us_per_call_unsplit"] = by_splits[1]
+        res["speedup_vs_unsplit"] = by_splits[1] / us
+    if cpu_seconds > 0:
+        res["cpu_baseline"] = _oracle_sample(c, sets, sl_h, bt_h, kv_bytes, cpu_seconds)
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
+# Every configuration of the method's five workloads (and the next rows'),
+# measured on the default bench line beside the headline: (label, workload,
+# batch, ctx, forced split counts, time n_splits = 1 too).
+CONFIGS = (
+    ("tiny_mha", "tiny_mha", None, None, (1, 3, 7), False),
+    ("varlen_b16", "varlen_b16", None, None, (), False),
+    ("paged_b8", "paged_b8", None, None, (), False),
+    ("sweep_b1_8k", "sweep", 1, 8192, (), True),
+    ("sweep_b1_128k", "sweep", 1, 131072, (), True),
+    ("sweep_b16_8k", "sweep", 16, 8192, (), True),
+    ("sweep_b16_128k", "sweep", 16, 131072, (), True),
+    ("long_gqa_128k_fp8", "long_gqa_128k_fp8", None, None, (), False),
+    ("query_block_q4", "query_block_q4", None, None, (), False),
+    ("query_block_g8_q4", "query_block_g8_q4", None, None, (), False),
+    ("query_block_g8_q8", "query_block_g8_q8", None, None, (), False),
+    ("query_block_g16_q8", "query_block_g16_q8", None, None, (), False),
+)
+
+
+def measure_configs(dev, stream, peak, eager, with_cpu):
+    import fd_inputs
+    out = {}
+    for label, name, batch, ctx, forced, unsplit in CONFIGS:
+        c = fd_inputs.WORKLOADS[name]
+        out[label] = measure_problem(name, c, dev, stream, peak, batch=batch, ctx=ctx, forced=forced,
+                                     unsplit=unsplit, eager=eager,
+                                     cpu_seconds=1.0 if with_cpu else 0.0)
+    return out
 
 
 def run_suite(args):
     """One JSON line per problem of a workload: device time per fd_decode call
     (inputs rotated across distinct sets larger than the L2), K+V GB/s and the
     fraction of the measured HBM peak; the sweep also times n_splits = 1."""
-    import math as _m
-
-    import numpy as np
     import torch
 
     import fd_inputs
-    import split_kv_gb300 as fd
     from split_kv_gb300 import _build
     _build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     peak, peak_src = _peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     name = args.workload
     c = fd_inputs.WORKLOADS[name]
     grid = "batches" in c   # a sweep over batch x context
-    if grid:
-        probs = [(b, t) for b in c["batches"] for t in c["ctxs"]]
-        base = dict(c, batch=None, ctx=None, dtype=c["dtype"])
-    else:
-        probs = [(None, None)]
-        base = c
+    probs = [(b, t) for b in c["batches"] for t in c["ctxs"]] if grid else [(None, None)]
+    base = dict(c, batch=None, ctx=None) if grid else c
     for batch, ctx in probs:
-        B = batch or c["batch"]
-        T = ctx or c["ctx"]
-        per_set = None
-        est = B * c["n_kv_heads"] * T * c["head_dim"] * (2 if c.get("kv_dtype") == "e4m3" else 4)
-        n_sets = max(1, min(256, _m.ceil(4 * l2 / max(est, 1))))
-        sets, sl_h = _problem_sets(name, base, dev, n_sets, batch, ctx)
-        seqlens = torch.from_numpy(sl_h).to(dev)
-        esize = 1 if c.get("kv_dtype") == "e4m3" else 2
-        kv_bytes = int(sl_h.sum()) * c["n_kv_heads"] * c["head_dim"] * esize * 2
-        ql = c.get("q_len", 1)
-        cols = (c["n_q_heads"] // c["n_kv_heads"]) * ql
-        umma = c.get("kv_dtype") != "e4m3" and not args.cuda_cores and 16 < cols <= 128
-        cblocks = 1 if (umma or cols <= 8) else -(-cols // 16)     # CTAs per split (query blocks)
-        S_plan = fd.fd_plan_splits(B * c["n_kv_heads"] * cblocks, (1 if umma else 2) * fd.fd_num_sms(),
-                                   -(-int(sl_h.max()) // 128))
-        if ql == 1:
-            assert S_plan == fd.fd_plan(B, c["n_q_heads"], c["n_kv_heads"], c["head_dim"], sl_h)
-        results = {}
-        for label, S in (("planned", S_plan), ("unsplit", 1)):
-            if label == "unsplit" and (not grid or S_plan == 1):
-                continue   # with a one-split plan the two are the same launch
-            descs = []
-            for (desc, q, k, v, bt) in sets:
-                d = desc.copy()
-                d.n_splits = S
-                if args.cuda_cores:
-                    d.flags = fd.FD_FLAG_CUDA_CORES
-                descs.append(d)
-            wsb = fd.fd_workspace_size(descs[0], S)
-            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            out = torch.empty(B, ql, c["n_q_heads"], c["head_dim"], dtype=torch.float32, device=dev)
-            lse = torch.empty(B, ql, c["n_q_heads"], dtype=torch.float32, device=dev)
-
-            def call(j, h):
-                _, q, k, v, bt = sets[j]
-                rc = fd.fd_decode(descs[j], q, k, v, seqlens, bt, out, lse, ws, wsb, stream=h)
-                if rc != 0:
-                    raise fd.FdError(rc, "fd_decode")
-
-            # at least 50 calls (several ms of timed work even for the smallest problems)
-            iters = max(50, min(2000, int(1e10 / max(kv_bytes, 1))))
-            ms, note = _time_calls(call, n_sets, iters, max(3, args.warmup), stream, dev, args.eager)
-            results[label] = (S, ms)
-        fd.check(fd.fd_device_status(stream), "device status")
-        S, ms = results["planned"]
-        line = {"workload": name, "batch": B, "ctx": T, "q_len": ql, "n_q_heads": c["n_q_heads"],
-                "n_kv_heads": c["n_kv_heads"], "kv_dtype": c.get("kv_dtype", c["dtype"]), "n_splits": S,
-                "us_per_call": ms * 1e3, "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
-                "frac_of_hbm_peak": kv_bytes / (ms * 1e-3) / 1e9 / peak, "peak_source": peak_src,
-                "input_sets": n_sets, "kv_bytes": kv_bytes, "launch": note,
-                "split_compute": "cuda_cores" if args.cuda_cores else "tensor_cores"}
-        if grid:
-            S1, ms1 = results.get("unsplit", results["planned"])
-            line["us_per_call_unsplit"] = ms1 * 1e3
-            line["kv_gbs_unsplit"] = kv_bytes / (ms1 * 1e-3) / 1e9
-            line["speedup_vs_unsplit"] = ms1 / ms
+        line = measure_problem(name, base, dev, stream, peak, batch=batch, ctx=ctx, unsplit=grid,
+                               eager=args.eager, cuda_cores=args.cuda_cores, warmup=args.warmup)
+        line["peak_source"] = peak_src
+        line["split_compute"] = "cuda_cores" if args.cuda_cores else "tensor_cores"
         print(json.dumps(line), flush=True)
-        del sets
-        torch.cuda.empty_cache()
 
 
 def main():

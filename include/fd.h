@@ -63,9 +63,11 @@
 extern "C" {
 #endif
 
-#define FD_ABI_VERSION 3
+#define FD_ABI_VERSION 4
 #define FD_MAX_SPLITS 128   /* the split-count heuristic's cap ("Flash-Decoding ...", §6) */
-#define FD_TILE_TOKENS 128  /* split ranges are whole 128-token tiles; the planner's KV block */
+#define FD_TILE_TOKENS 128  /* the planner's KV block: n_kv_blocks = ceil(max seqlen / 128)
+                               ("Flash-Decoding ...", §6).  Split ranges themselves are
+                               balanced whole 16-token units (8 for 8-token pages). */
 
 typedef enum fd_status {
     FD_OK = 0,
@@ -160,20 +162,49 @@ int32_t fd_num_sms(int32_t device);
 int32_t fd_plan_splits(int64_t work_items, int64_t slots, int64_t n_kv_blocks,
                        int32_t max_splits);
 
-/* n_splits for one decode step with one query position per sequence:
- * fd_plan_splits(batch*n_kv_heads, 2*num_sms,
- * ceil(max_b seqlens_host[b] / 128), 128).  work is KV heads x batch because a
- * CTA serves a whole GQA group ("Flash-Decoding ...", §1 GQA note); two slots
- * per SM as in the page's §6 dispatcher.  seqlens_host: host array of `batch`
- * lengths (>= 0).  num_sms <= 0 queries the current device.  The result
- * depends only on batch, n_kv_heads, max seqlen and num_sms; n_q_heads and
- * head_dim are validated only.  Returns s in [1, 128] or a negative fd_status.
- * (fd_decode, given n_splits <= 0, plans query blocks the same way with
- * work = the CTAs per split: batch*n_kv_heads for up to 16 columns, and for
- * the tcgen05 tile of 17-128 columns (16-bit cache), whose CTA fills an SM,
- * with slots = num_sms; batch*n_kv_heads*ceil(G*q_len/16) otherwise.) */
+/* n_splits for one decode step ("Flash-Decoding ...", §6 "How many splits?",
+ * and its §9 decode contract, which plans before launch from the host-known
+ * lengths and, for a paged cache, the block table).
+ * It is the split count fd_decode plans for this shape with a 16-bit cache on
+ * the default (tensor-core) path and one query position per sequence:
+ *     fd_plan_splits(work, slots, ceil(max_b seqlens_host[b] / 128), 128)
+ * with G = n_q_heads / n_kv_heads and
+ *   - G <= 16: work = batch*n_kv_heads (a CTA serves the whole GQA group,
+ *     "Flash-Decoding ...", §1 GQA note) and slots = 2*num_sms (two CTAs per
+ *     SM, as the page's §6 dispatcher passes);
+ *   - 16 < G <= 128: the tcgen05 CTA of all G columns fills an SM, so
+ *     work = batch*n_kv_heads and slots = num_sms;
+ *   - G > 128: one CTA per 16 columns, work = batch*n_kv_heads*ceil(G/16),
+ *     slots = 2*num_sms.
+ * For an fp8 cache, query blocks or FD_FLAG_CUDA_CORES use fd_plan_desc.
+ *  seqlens_host      : host int32[batch], lengths >= 0.
+ *  block_table_host  : host int32[batch*max_pages_per_seq] of a paged cache, or
+ *                      NULL.  It never changes the plan; when given it is
+ *                      validated: page_size a power of two >= 8, and for every
+ *                      sequence b, ceil(seqlens[b]/page_size) <= max_pages_per_seq
+ *                      and those entries >= 0 (the pool size is not known
+ *                      here; the kernel checks the upper bound).
+ *  page_size, max_pages_per_seq : the paged layout (fd_desc); ignored when
+ *                      block_table_host is NULL.
+ *  num_sms           : <= 0 queries the current device.
+ * The result depends only on batch, G, n_kv_heads, max seqlen and num_sms;
+ * head_dim is validated only.  Returns s in [1, 128], or FD_ERR_INVALID_ARG
+ * (bad shape, a negative length, a table that misses a page),
+ * FD_ERR_UNSUPPORTED (G > 256, 1 < page_size < 8) or FD_ERR_CUDA (no device
+ * to count SMs on). */
 int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                const int32_t* seqlens_host, int32_t num_sms);
+                const int32_t* seqlens_host, const int32_t* block_table_host,
+                int32_t page_size, int32_t max_pages_per_seq, int32_t num_sms);
+
+/* The split count fd_decode uses for `desc` when desc->n_splits <= 0 and
+ * desc->max_seqlen = max_b seqlens_host[b]: the rule of fd_plan with the
+ * CTAs per split of this descriptor's kernel -- G*q_len columns per KV head;
+ * one CTA per split up to 16 columns, or for 17-128 columns on a 16-bit
+ * cache without FD_FLAG_CUDA_CORES (then one slot per SM); otherwise
+ * ceil(G*q_len/16) CTAs per split, two slots per SM.  desc->n_splits and
+ * desc->max_seqlen are ignored.  seqlens_host: host int32[desc->batch] >= 0.
+ * Returns s in [1, 128] or a negative fd_status. */
+int32_t fd_plan_desc(const fd_desc* desc, const int32_t* seqlens_host, int32_t num_sms);
 
 /* Bytes of workspace fd_decode needs for `n_splits` (<= 0: the split count
  * fd_decode would plan).  Layout (all fp32, each section 256-byte aligned,
@@ -226,8 +257,14 @@ fd_status fd_combine_states(const fd_desc* desc, const void* workspace, size_t w
 
 /* Reads (and with clear != 0 resets) the current device's status word after
  * synchronising `stream`.  FD_OK, FD_ERR_DEVICE_TIMEOUT, FD_ERR_DEVICE_BOUNDS
- * or FD_ERR_CUDA.  The word is sticky across calls until cleared. */
+ * or FD_ERR_CUDA.  The word is sticky across calls until cleared.  The word
+ * belongs to the current CUDA context (one per device in the usual case). */
 fd_status fd_device_status(void* stream, int32_t clear);
+
+/* The decode status call of the decode contract: fd_device_status(stream, 1),
+ * i.e. reads the conditions only the GPU can see (a timed-out wait, a length
+ * or page index out of range) and clears them. */
+fd_status fd_decode_status(void* stream);
 
 /* Size of the fixed device workspace behind fd_decode_static: 8 MiB, enough
  * for batch*n_q_heads*n_splits up to 16131 query-row splits at head_dim 128
@@ -247,12 +284,16 @@ fd_status fd_device_status(void* stream, int32_t clear);
  * until the process exits.
  *
  *  - It allocates nothing and frees nothing (no cudaMalloc, cudaFree or other
- *    allocating routine).  The first call on a device looks up the array's
- *    device address (cudaGetSymbolAddress) with that device current; make
- *    that first call before any stream capture on the device.
- *  - Problems whose workspace (fd_workspace_size) exceeds
- *    FD_STATIC_WORKSPACE_BYTES are rejected with FD_ERR_WORKSPACE before
- *    anything is enqueued.
+ *    allocating routine).  The first call in a CUDA context (normally: on a
+ *    device) looks up the array's device address (cudaGetSymbolAddress) with
+ *    that context current, and keeps it for that context; make that first
+ *    call before any stream capture.  A context destroyed and created again
+ *    (cudaDeviceReset) counts as a new one and is looked up again.
+ *  - Problems with more than one split whose workspace (fd_workspace_size)
+ *    exceeds FD_STATIC_WORKSPACE_BYTES are rejected with FD_ERR_WORKSPACE
+ *    before anything is enqueued.  With one split (given, or planned) the
+ *    split kernel writes out and lse itself and the array is not used, so
+ *    no size limit applies.
  *  - Every call on a device shares the one array, and the array keeps what
  *    the last call left in it.  The split kernel overwrites every state the
  *    combine reads, so nothing needs clearing between calls, but calls whose

@@ -44,8 +44,8 @@ LIB_PATH = _build.LIB_PATH
 
 # every function the header declares (checked against include/fd.h by the tests)
 EXPORTS = ("fd_abi_version", "fd_status_string", "fd_num_sms", "fd_plan_splits", "fd_plan",
-           "fd_workspace_size", "fd_decode", "fd_split_states", "fd_combine_states",
-           "fd_device_status", "fd_decode_static")
+           "fd_plan_desc", "fd_workspace_size", "fd_decode", "fd_split_states", "fd_combine_states",
+           "fd_device_status", "fd_decode_status", "fd_decode_static")
 
 
 class FdDesc(ctypes.Structure):
@@ -103,12 +103,14 @@ def _load():
             "fd_status_string": (ctypes.c_char_p, [i32]),
             "fd_num_sms": (i32, [i32]),
             "fd_plan_splits": (i32, [i64, i64, i64, i32]),
-            "fd_plan": (i32, [i32, i32, i32, i32, vp, i32]),
+            "fd_plan": (i32, [i32, i32, i32, i32, vp, vp, i32, i32, i32]),
+            "fd_plan_desc": (i32, [dp, vp, i32]),
             "fd_workspace_size": (sz, [dp, i32]),
             "fd_decode": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "fd_split_states": (i32, [dp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "fd_combine_states": (i32, [dp, vp, sz, vp, vp, vp]),
             "fd_device_status": (i32, [vp, i32]),
+            "fd_decode_status": (i32, [vp]),
             "fd_decode_static": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -162,13 +164,38 @@ def fd_plan_splits(work_items: int, slots: int, n_kv_blocks: int, max_splits: in
     return int(_load().fd_plan_splits(int(work_items), int(slots), int(n_kv_blocks), int(max_splits)))
 
 
+def _host_i32(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32).reshape(-1))
+
+
 def fd_plan(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, seqlens_host,
-            num_sms: int = 0) -> int:
-    sl = np.ascontiguousarray(np.asarray(seqlens_host, dtype=np.int32).reshape(-1))
+            num_sms: int = 0, *, block_table_host=None, page_size: int = 0) -> int:
+    """Split count for one decode step (16-bit cache, one query per sequence).
+    block_table_host: optional host [batch, max_pages_per_seq] int32 table of
+    a paged cache with `page_size`-token pages; validated, never changes the plan."""
+    sl = _host_i32(seqlens_host)
     if sl.shape[0] < batch:
         raise ValueError("seqlens_host shorter than batch")
-    return int(_load().fd_plan(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim),
-                               sl.ctypes.data if batch > 0 else None, int(num_sms)))
+    bt_ptr, mp = None, 0
+    if block_table_host is not None:
+        bt = np.ascontiguousarray(np.asarray(block_table_host, dtype=np.int32))
+        if bt.ndim != 2 or bt.shape[0] < batch:
+            raise ValueError("block_table_host must be [batch, max_pages_per_seq]")
+        mp = bt.shape[1]
+        bt_ptr = bt.ctypes.data
+    r = _load().fd_plan(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim),
+                        sl.ctypes.data if batch > 0 else None, bt_ptr, int(page_size), int(mp),
+                        int(num_sms))
+    return int(r)
+
+
+def fd_plan_desc(desc: FdDesc, seqlens_host, num_sms: int = 0) -> int:
+    """The split count fd_decode plans for `desc` (n_splits <= 0) with these lengths."""
+    sl = _host_i32(seqlens_host)
+    if sl.shape[0] < desc.batch:
+        raise ValueError("seqlens_host shorter than batch")
+    return int(_load().fd_plan_desc(ctypes.byref(desc), sl.ctypes.data if desc.batch > 0 else None,
+                                    int(num_sms)))
 
 
 def fd_workspace_size(desc: FdDesc, n_splits: int = 0) -> int:
@@ -202,8 +229,8 @@ def fd_decode_static(desc: FdDesc, q, k_cache, v_cache, seqlens, block_table, ou
                      stream=None) -> int:
     """fd_decode without a caller workspace: for callers that cannot allocate
     device memory; the states go to the library's fixed device array
-    (FD_STATIC_WORKSPACE_BYTES per GPU).  Calls that overlap on the GPU race
-    on that array."""
+    (FD_STATIC_WORKSPACE_BYTES per GPU; not used at all with one split).
+    Calls that overlap on the GPU race on that array."""
     return int(_load().fd_decode_static(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(seqlens), _ptr(block_table), _ptr(out), _ptr(lse),
                                         _stream(stream)))
@@ -211,6 +238,10 @@ def fd_decode_static(desc: FdDesc, q, k_cache, v_cache, seqlens, block_table, ou
 
 def fd_device_status(stream=None, clear: bool = True) -> int:
     return int(_load().fd_device_status(_stream(stream), 1 if clear else 0))
+
+
+def fd_decode_status(stream=None) -> int:
+    return int(_load().fd_decode_status(_stream(stream)))
 
 
 # ---------------------------------------------------------------- helpers

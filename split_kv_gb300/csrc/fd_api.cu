@@ -111,12 +111,8 @@ fd_status check_desc(const fd_desc* d) {
 // Split count a call uses: the descriptor's, or the planner's.
 int32_t splits_for(const fd_desc* d) {
     if (d->n_splits >= 1) return d->n_splits;
-    const int32_t sms = fd_num_sms(-1);
-    if (sms < 0) return sms;
-    const int64_t blocks = (static_cast<int64_t>(d->max_seqlen) + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS;
-    // two CTAs per SM, or one for the tcgen05 variant
-    return fd_plan_splits(static_cast<int64_t>(d->batch) * d->n_kv_heads * col_blocks_of(d),
-                          (umma_of(d) ? 1 : 2) * static_cast<int64_t>(sms), blocks, FD_MAX_SPLITS);
+    return fdk::plan_launch(d->batch, d->n_kv_heads, cols_of(d), is_fp8(d),
+                            (d->flags & FD_FLAG_CUDA_CORES) != 0, d->max_seqlen, 0);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -136,6 +132,19 @@ EncodeTiledFn encode_fn() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
+}
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<Fn>(p);
+    return nullptr;
 }
 
 // 4-D map over one cache: dims (head_dim, tokens, kv heads, sequences|pages),
@@ -174,7 +183,10 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
                      const int32_t* seqlens, const int32_t* block_table, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream, bool direct = false,
                      void* out = nullptr, float* lse = nullptr) {
-    if (q == nullptr || k == nullptr || v == nullptr || seqlens == nullptr || workspace == nullptr)
+    // a direct one-split launch given no workspace never touches one
+    const bool no_ws = direct && S == 1 && out != nullptr && workspace == nullptr;
+    if (q == nullptr || k == nullptr || v == nullptr || seqlens == nullptr ||
+        (workspace == nullptr && !no_ws))
         return FD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FD_ERR_INVALID_ARG;
     const bool paged = d->page_size > 0;
@@ -182,7 +194,7 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     const int64_t rows = rows_of(d);
     const WsLayout w = ws_layout(rows, S);
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FD_ERR_WORKSPACE;
-    if (workspace_bytes < w.total) return FD_ERR_WORKSPACE;
+    if (!no_ws && workspace_bytes < w.total) return FD_ERR_WORKSPACE;
     if (d->batch == 0) return FD_OK;
     if (d->batch > 65535 || d->n_kv_heads > 65535)   // grid (S * col_blocks, n_kv_heads, batch)
         return FD_ERR_UNSUPPORTED;
@@ -223,9 +235,9 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
                                             (is_fp8(d) ? static_cast<double>(d->k_scale) : 1.0));
     p.v_scale = is_fp8(d) ? d->v_scale : 1.0f;
     char* ws = static_cast<char*>(workspace);
-    p.ws_u = reinterpret_cast<float*>(ws + w.off_u);
-    p.ws_m = reinterpret_cast<float*>(ws + w.off_m);
-    p.ws_l = reinterpret_cast<float*>(ws + w.off_l);
+    p.ws_u = no_ws ? nullptr : reinterpret_cast<float*>(ws + w.off_u);
+    p.ws_m = no_ws ? nullptr : reinterpret_cast<float*>(ws + w.off_m);
+    p.ws_l = no_ws ? nullptr : reinterpret_cast<float*>(ws + w.off_l);
     p.direct = direct && S == 1 && out != nullptr ? 1 : 0;
     p.out_dtype = d->out_dtype == FD_F16 ? 0 : d->out_dtype == FD_BF16 ? 1 : 2;
     p.out = out;
@@ -264,29 +276,60 @@ fd_status combine_impl(const fd_desc* d, int32_t S, const void* workspace, size_
 // buffer.  Every device that loads the library holds this array until exit.
 static __device__ __align__(256) unsigned char g_static_workspace[FD_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxStaticDevices = 64;
+// The array's device address in each CUDA context that used it, looked up
+// once per context: the address belongs to the context, and a context that
+// is destroyed and created again (cudaDeviceReset) may place it elsewhere.
+// (In host code the symbol is only a host-side stand-in; handing it to a
+// kernel would read the wrong memory.)
+constexpr int kStaticSlots = 64;
 std::mutex g_static_mutex;
-void* g_static_ptr[kMaxStaticDevices] = {};
+unsigned long long g_static_ctx[kStaticSlots] = {};
+void* g_static_ptr[kStaticSlots] = {};
+int g_static_next = 0;
 
-// Device address of g_static_workspace on the current device, looked up once
-// per device.  (In host code the symbol is only a host-side stand-in; handing
-// it to a kernel would read the wrong memory.)
 fd_status static_workspace(void** ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FD_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxStaticDevices) return FD_ERR_UNSUPPORTED;
+    const unsigned long long ctx = fdk::current_context_id();
     std::lock_guard<std::mutex> lock(g_static_mutex);
-    if (g_static_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr)
-            return FD_ERR_CUDA;
-        g_static_ptr[dev] = p;
+    if (ctx != 0) {
+        for (int i = 0; i < kStaticSlots; ++i)
+            if (g_static_ctx[i] == ctx) {
+                *ptr = g_static_ptr[i];
+                return FD_OK;
+            }
     }
-    *ptr = g_static_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return FD_ERR_CUDA;
+    if (ctx != 0) {   // without a context id every call looks the address up again
+        g_static_ctx[g_static_next] = ctx;
+        g_static_ptr[g_static_next] = p;
+        g_static_next = (g_static_next + 1) % kStaticSlots;
+    }
+    *ptr = p;
     return FD_OK;
 }
 
 }  // namespace
+
+namespace fdk {
+
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+        get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+}  // namespace fdk
 
 extern "C" {
 
@@ -357,17 +400,38 @@ fd_status fd_decode_static(const fd_desc* desc, const void* q, const void* k_cac
     if (out == nullptr) return FD_ERR_INVALID_ARG;
     const int32_t S = splits_for(desc);
     if (S < 1) return static_cast<fd_status>(S < 0 ? S : FD_ERR_INVALID_ARG);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (S == 1) {
+        // one split: the split kernel writes out and lse itself and uses no
+        // workspace, so neither the size limit nor the array applies
+        return split_impl(desc, 1, q, k_cache, v_cache, seqlens, block_table, nullptr, 0, s, true,
+                          out, lse);
+    }
     const size_t need = ws_layout(rows_of(desc), S).total;
     if (need > FD_STATIC_WORKSPACE_BYTES) return FD_ERR_WORKSPACE;
     void* ws = nullptr;
     st = static_workspace(&ws);
     if (st != FD_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = split_impl(desc, S, q, k_cache, v_cache, seqlens, block_table, ws,
-                    FD_STATIC_WORKSPACE_BYTES, s, S == 1, out, lse);
-    if (st != FD_OK || S == 1) return st;
+                    FD_STATIC_WORKSPACE_BYTES, s, false, out, lse);
+    if (st != FD_OK) return st;
     return combine_impl(desc, S, ws, FD_STATIC_WORKSPACE_BYTES, out, lse, s);
 }
+
+int32_t fd_plan_desc(const fd_desc* desc, const int32_t* seqlens_host, int32_t num_sms) {
+    fd_status st = check_desc(desc);
+    if (st != FD_OK) return st;
+    if (desc->batch < 1 || seqlens_host == nullptr) return FD_ERR_INVALID_ARG;
+    int64_t max_len = 0;
+    for (int32_t b = 0; b < desc->batch; ++b) {
+        if (seqlens_host[b] < 0) return FD_ERR_INVALID_ARG;
+        if (seqlens_host[b] > max_len) max_len = seqlens_host[b];
+    }
+    return fdk::plan_launch(desc->batch, desc->n_kv_heads, cols_of(desc), is_fp8(desc),
+                            (desc->flags & FD_FLAG_CUDA_CORES) != 0, max_len, num_sms);
+}
+
+fd_status fd_decode_status(void* stream) { return fd_device_status(stream, 1); }
 
 fd_status fd_device_status(void* stream, int32_t clear) {
     unsigned v = 0;

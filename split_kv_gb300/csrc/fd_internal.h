@@ -110,6 +110,21 @@ inline int column_blocks(int cols) { return cols <= 8 ? 1 : (cols + 15) / 16; }
 inline bool use_umma(bool fp8, bool cuda_cores, int cols) {
     return !fp8 && !cuda_cores && cols > 16 && cols <= 128;
 }
+
+// Split count of one split-kernel launch by the wave-efficiency heuristic
+// (fd_plan_splits): work = the launch's CTAs per split (column blocks, or one
+// tcgen05 CTA) x n_kv_heads x batch; slots = the CTAs the GPU holds at once,
+// two per SM, or one per SM for the tcgen05 variant; n_kv_blocks =
+// ceil(max_seqlen / 128).  cols = G * q_len.  num_sms <= 0 queries the
+// current device.  Returns s >= 1 or a negative fd_status.
+int32_t plan_launch(int64_t batch, int64_t n_kv_heads, int cols, bool fp8, bool cuda_cores,
+                    int64_t max_seqlen, int32_t num_sms);
+
+// Identifier of the CUDA context current on the calling thread, unique per
+// context creation (a context destroyed and created again gets a new one);
+// 0 when no context is current or the driver cannot say.  Per-context state
+// (the fixed workspace's address, kernel attributes) is keyed on it.
+unsigned long long current_context_id();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 // Device status word helpers (fd_split.cu owns the symbol).

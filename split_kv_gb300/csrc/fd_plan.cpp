@@ -22,6 +22,7 @@
 #include <cstdint>
 
 #include "../../include/fd.h"
+#include "fd_internal.h"
 
 namespace {
 
@@ -69,21 +70,55 @@ extern "C" int32_t fd_num_sms(int32_t device) {
     return n;
 }
 
-extern "C" int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                           const int32_t* seqlens_host, int32_t num_sms) {
-    if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return FD_ERR_INVALID_ARG;
-    if (n_q_heads % n_kv_heads != 0 || seqlens_host == nullptr) return FD_ERR_INVALID_ARG;
-    int64_t max_len = 0;
-    for (int32_t b = 0; b < batch; ++b) {
-        if (seqlens_host[b] < 0) return FD_ERR_INVALID_ARG;
-        max_len = std::max<int64_t>(max_len, seqlens_host[b]);
-    }
+namespace fdk {
+
+int32_t plan_launch(int64_t batch, int64_t n_kv_heads, int cols, bool fp8, bool cuda_cores,
+                    int64_t max_seqlen, int32_t num_sms) {
+    if (batch < 1 || n_kv_heads < 1 || cols < 1 || max_seqlen < 0) return FD_ERR_INVALID_ARG;
     int32_t sms = num_sms;
     if (sms <= 0) {
         sms = fd_num_sms(-1);
         if (sms < 0) return sms;
     }
-    const int64_t blocks = (max_len + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS;
-    return fd_plan_splits(static_cast<int64_t>(batch) * n_kv_heads, 2 * static_cast<int64_t>(sms),
+    // one CTA per split serves the whole group: up to 16 columns on warp MMAs,
+    // or 17-128 on the tcgen05 variant, whose shared memory fills an SM;
+    // otherwise one CTA per 16 columns, two CTAs per SM
+    const bool umma = use_umma(fp8, cuda_cores, cols);
+    const int64_t per_split = umma ? 1 : column_blocks(cols);
+    const int64_t blocks = (max_seqlen + FD_TILE_TOKENS - 1) / FD_TILE_TOKENS;
+    return fd_plan_splits(batch * n_kv_heads * per_split, (umma ? 1 : 2) * static_cast<int64_t>(sms),
                           blocks, FD_MAX_SPLITS);
+}
+
+}  // namespace fdk
+
+extern "C" int32_t fd_plan(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                           const int32_t* seqlens_host, const int32_t* block_table_host,
+                           int32_t page_size, int32_t max_pages_per_seq, int32_t num_sms) {
+    if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || head_dim < 1) return FD_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0 || seqlens_host == nullptr) return FD_ERR_INVALID_ARG;
+    const int64_t G = n_q_heads / n_kv_heads;
+    if (G > 256) return FD_ERR_UNSUPPORTED;
+    if (block_table_host != nullptr) {
+        if (page_size < 8 || (page_size & (page_size - 1)) != 0 || page_size > (1 << 20))
+            return page_size >= 1 && page_size < 8 && (page_size & (page_size - 1)) == 0
+                       ? FD_ERR_UNSUPPORTED
+                       : FD_ERR_INVALID_ARG;
+        if (max_pages_per_seq < 1) return FD_ERR_INVALID_ARG;
+    }
+    int64_t max_len = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t L = seqlens_host[b];
+        if (L < 0) return FD_ERR_INVALID_ARG;
+        max_len = std::max<int64_t>(max_len, L);
+        if (block_table_host == nullptr) continue;
+        // the table must name a page for every token of the sequence
+        const int64_t need = (static_cast<int64_t>(L) + page_size - 1) / page_size;
+        if (need > max_pages_per_seq) return FD_ERR_INVALID_ARG;
+        const int32_t* row = block_table_host + static_cast<int64_t>(b) * max_pages_per_seq;
+        for (int64_t j = 0; j < need; ++j)
+            if (row[j] < 0) return FD_ERR_INVALID_ARG;
+    }
+    // a 16-bit cache on the default (tensor-core) path, one query per sequence
+    return fdk::plan_launch(batch, n_kv_heads, static_cast<int>(G), false, false, max_len, num_sms);
 }

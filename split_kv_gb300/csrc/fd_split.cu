@@ -38,6 +38,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "fd_device.cuh"
 #include "fd_internal.h"
 
@@ -1894,22 +1896,28 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Raises the dynamic shared-memory limit of `kern` to `smem`, once per CUDA
+// context (the attribute belongs to the context's copy of the kernel).  With
+// no readable context id it is set on every launch; the call is idempotent.
+template <typename Kern>
+static cudaError_t allow_smem(Kern kern, size_t smem, std::atomic<unsigned long long>& configured_ctx) {
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && configured_ctx.load(std::memory_order_acquire) == ctx) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess && ctx != 0) configured_ctx.store(ctx, std::memory_order_release);
+    return e;
+}
+
 template <typename T, int KIND>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
     auto kern = fd_split_kernel<T, KIND>;
     const size_t smem = Geo<KIND>::kSmem;
-    // one attribute call per (kernel, device): cheap and safe to repeat
-    static thread_local int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
+    static std::atomic<unsigned long long> configured_ctx{0};
+    cudaError_t e = allow_smem(kern, smem, configured_ctx);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
                       dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
@@ -1946,15 +1954,9 @@ static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& 
                                     int batch, int n_kv_heads, cudaStream_t stream) {
     auto kern = KIND == 32 ? fd_split_umma64_kernel<T> : fd_split_umma_kernel<T>;
     const size_t smem = Geo<KIND>::kSmem;
-    static thread_local int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
+    static std::atomic<unsigned long long> configured_ctx{0};
+    cudaError_t e = allow_smem(kern, smem, configured_ctx);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
                       dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }

@@ -7,6 +7,7 @@ import torch
 
 import oracle
 import split_kv_gb300 as fd
+from plan_model import slot_model
 
 GUARD = 256          # guard elements (or bytes) on each side of every written buffer
 ATOL, RTOL = 2e-3, 1e-2
@@ -71,7 +72,9 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
         # the planner's rule with the CTAs per split of this query block
         S = planned_splits(B, Hq, desc.n_kv_heads, ql, seqlens_h, fp8=desc.kv_dtype == fd.FD_E4M3,
                            cuda_cores=(flags & fd.FD_FLAG_CUDA_CORES) != 0)
-        if ql == 1:
+        if B > 0:
+            assert S == fd.fd_plan_desc(desc, seqlens_h)
+        if B > 0 and ql == 1 and desc.kv_dtype != fd.FD_E4M3 and not flags & fd.FD_FLAG_CUDA_CORES:
             assert S == fd.fd_plan(B, Hq, desc.n_kv_heads, D, seqlens_h)
     assert S >= 1
     desc.n_splits = 0 if n_splits <= 0 else S
@@ -94,15 +97,11 @@ def run_decode(q, k, v, seqlens_h, *, n_kv_heads=None, page_size=0, block_table=
 
 
 def planned_splits(B, Hq, Hkv, q_len, seqlens_h, fp8=False, cuda_cores=False):
-    """n_splits fd_decode plans: work = CTAs per split (column blocks of 16,
-    or one CTA of the tcgen05 variant for 16 < G*q_len <= 128 on a 16-bit
-    cache) x KV heads x batch, slots = 2 CTAs per SM (1 for tcgen05)."""
-    cols = (Hq // Hkv) * q_len
-    umma = not fp8 and not cuda_cores and 16 < cols <= 128
-    cb = 1 if (umma or cols <= 8) else -(-cols // 16)
-    per_sm = 1 if umma else 2
+    """n_splits fd_decode should plan: the oracle's statement of the heuristic
+    fed the launch shape of plan_model (this GPU's SM count)."""
+    work, slots = slot_model(B, Hkv, Hq // Hkv, q_len, fp8, cuda_cores, fd.fd_num_sms())
     blocks = -(-int(np.max(seqlens_h)) // 128) if B else 0
-    return fd.fd_plan_splits(B * Hkv * cb, per_sm * fd.fd_num_sms(), blocks)
+    return oracle.num_splits_ref(work, slots, blocks)
 
 
 def assert_parity(got_o, got_l, ref_o, ref_l, what=""):

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+from plan_model import slot_model
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -37,7 +38,7 @@ def test_library_exports_every_declared_symbol(fd):
 
 
 def test_abi_version_and_strings(fd):
-    assert fd.fd_abi_version() == 3
+    assert fd.fd_abi_version() == 4
     for code in range(-6, 1):
         s = fd.fd_status_string(code)
         assert s and s != "unknown status"
@@ -100,6 +101,81 @@ def test_plan_rejects_bad_arguments(fd):
     assert fd.fd_plan(1, 32, 6, 128, [10], 148) == fd.FD_ERR_INVALID_ARG    # 6 does not divide 32
     assert fd.fd_plan(2, 32, 8, 128, [10, -1], 148) == fd.FD_ERR_INVALID_ARG
     assert fd.fd_plan(1, 32, 8, 128, [0], 148) == 1                        # empty sequence
+
+
+def test_plan_validates_an_optional_page_table(fd):
+    """The decode contract plans from host lengths and, for a paged cache,
+    the block table: a table never changes the plan, a table that misses a
+    page or holds a negative page index where the sequence reaches is
+    rejected."""
+    sl = [100, 33, 0]
+    bt = np.arange(3 * 8, dtype=np.int32).reshape(3, 8)
+    want = fd.fd_plan(3, 32, 8, 128, sl, 148)
+    assert want == oracle.num_splits_ref(24, 296, 1)
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=bt, page_size=16) == want
+    for ps in (16, 64, 128):      # 100 tokens take 7, 2 and 1 of the 8 pages a row has
+        assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=bt, page_size=ps) == want
+    # 100 tokens need 13 pages of 8 but a row has 8
+    small = np.zeros((3, 8), dtype=np.int32)
+    assert fd.fd_plan(3, 32, 8, 128, [100, 1, 1], 148, block_table_host=small[:, :8],
+                      page_size=8) == fd.FD_ERR_INVALID_ARG
+    neg = bt.copy()
+    neg[1, 2] = -1      # sequence 1 (33 tokens, 16-token pages) reaches page 2
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=neg, page_size=16) == fd.FD_ERR_INVALID_ARG
+    neg = bt.copy()
+    neg[1, 3] = -1      # ... but not page 3: unused entries are not read
+    neg[2, 0] = -7      # and the empty sequence reads none
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=neg, page_size=16) == want
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=bt, page_size=12) == fd.FD_ERR_INVALID_ARG
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=bt, page_size=4) == fd.FD_ERR_UNSUPPORTED
+    assert fd.fd_plan(3, 32, 8, 128, sl, 148, block_table_host=bt, page_size=0) == fd.FD_ERR_INVALID_ARG
+
+
+def test_plan_desc_follows_the_slot_model_and_the_oracle(fd):
+    """fd_plan_desc (the plan of fd_decode) against the oracle's statement of
+    the heuristic fed the slot model above, over dtypes, flags, group sizes
+    and query blocks; fd_plan is the same plan for a 16-bit cache, one query."""
+    rng = np.random.default_rng(5)
+    checked = 0
+    for sms in (132, 148, 152):
+        for G in (1, 2, 3, 4, 8, 16, 17, 24, 32, 64, 100, 128, 129, 256):
+            for q_len in (1, 2, 4, 8, 16):
+                if G * q_len > 256:
+                    continue
+                for fp8 in (False, True):
+                    for cc in (False, True):
+                        if cc and (fp8 or q_len != 1 or G not in (1, 2, 4, 8)):
+                            continue
+                        B = int(rng.integers(1, 20))
+                        Hkv = int(rng.integers(1, 9))
+                        L = rng.integers(0, 300000, size=B).astype(np.int32)
+                        kw = dict(batch=B, n_q_heads=G * Hkv, n_kv_heads=Hkv, q_len=q_len,
+                                  q_stride_t=G * Hkv * 128, q_stride_b=q_len * G * Hkv * 128,
+                                  flags=fd.FD_FLAG_CUDA_CORES if cc else 0)
+                        if fp8:
+                            kw.update(kv_dtype=fd.FD_E4M3, q_dtype=fd.FD_F16, k_scale=1.0, v_scale=1.0)
+                        d = _desc(fd, **kw)
+                        work, slots = slot_model(B, Hkv, G, q_len, fp8, cc, sms)
+                        want = oracle.num_splits_ref(work, slots, -(-int(L.max()) // 128))
+                        assert fd.fd_plan_desc(d, L, sms) == want, (sms, G, q_len, fp8, cc, B, Hkv)
+                        if q_len == 1 and not fp8 and not cc:
+                            assert fd.fd_plan(B, G * Hkv, Hkv, 128, L, sms) == want
+                        checked += 1
+    assert checked > 300
+
+
+def test_plan_of_wide_groups_matches_the_launch(fd):
+    """A single query with 32 heads per KV head runs the tcgen05 CTA (one per
+    SM): 16 sequences x 8 KV heads = 128 CTAs already cover 0.8 of 152 slots,
+    so neither fd_plan nor fd_decode splits."""
+    L = [131072] * 16
+    assert fd.fd_plan(16, 256, 8, 128, L, 152) == 1
+    d = _desc(fd, batch=16, n_q_heads=256, n_kv_heads=8, q_stride_b=256 * 128)
+    assert fd.fd_plan_desc(d, L, 152) == 1
+    # the same group over an fp8 cache: two column blocks per split, two slots per SM
+    d8 = _desc(fd, batch=16, n_q_heads=256, n_kv_heads=8, q_stride_b=256 * 128,
+               kv_dtype=fd.FD_E4M3, q_dtype=fd.FD_BF16, k_scale=1.0, v_scale=1.0)
+    assert fd.fd_plan_desc(d8, L, 152) == oracle.num_splits_ref(16 * 8 * 2, 304, 1024)
 
 
 def _desc(fd, **kw):

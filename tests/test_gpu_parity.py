@@ -420,6 +420,8 @@ def test_paged_b8_full_sampled_rows():
     q = fd_inputs.randn((B, Hq, D), c["dtype"], c["seed"] + 3, device=DEV)
     sl = np.full(B, T, dtype=np.int32)
     got_o, got_l, S = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt)
+    # the decode contract's planner, given the host block table, plans the same
+    assert S == fd.fd_plan(B, Hq, Hkv, D, sl, block_table_host=bt, page_size=ps)
     rows = np.random.default_rng(5).choice(B * Hq, size=64, replace=False)
     ref_o, ref_l = oracle_all(q, pk, pv, sl, c["dtype"], Hkv, page_size=ps, block_table=bt, rows=rows)
     assert_parity(got_o[rows], got_l[rows], ref_o, ref_l, f"paged_b8 S={S}")
