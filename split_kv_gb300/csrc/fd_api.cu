@@ -224,6 +224,8 @@ fd_status split_impl(const fd_desc* d, int32_t S, const void* q, const void* k, 
     p.capacity = paged ? d->max_pages_per_seq * d->page_size : static_cast<int32_t>(d->kv_extent);
     p.n_pages = paged ? static_cast<int32_t>(d->kv_extent) : 0;
     p.n_q_heads = d->n_q_heads;
+    p.n_kv_heads = d->n_kv_heads;
+    p.batch = d->batch;
     p.n_splits = S;
     // whole 16-token units (8-token pages: 8), the paged box height, so a
     // TMA box never crosses a page and paged and contiguous caches split alike

@@ -41,6 +41,8 @@ struct SplitParams {
     int32_t capacity;               // tokens a sequence may hold
     int32_t n_pages;                // paged pool size
     int32_t n_q_heads;
+    int32_t n_kv_heads;
+    int32_t batch;
     int32_t group;                  // G = query heads per KV head
     int32_t q_len;                  // query positions per sequence
     int32_t cols;                   // G * q_len (query position, head) columns per KV head

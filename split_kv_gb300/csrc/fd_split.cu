@@ -26,9 +26,10 @@
 //    consume_f8 builds the same MMAs' fragments from e4m3 bytes in registers;
 //    consume_simt (FD_FLAG_CUDA_CORES) uses FP32 FMAs, a half-warp per K row.
 //  - Query blocks of 17-128 columns on a 16-bit cache run instead on 5th-
-//    generation tensor cores (fd_split_umma64_kernel, fd_split_umma_kernel):
-//    one CTA per split holds every column as the M rows of tcgen05 MMAs with
-//    S and O accumulated in tensor memory, fed by the same TMA stages.
+//    generation tensor cores (fd_split_umma_kernel): a persistent grid of one
+//    CTA per SM serves the splits in turn, each holding every column as the M
+//    rows of tcgen05 MMAs with S and O accumulated in tensor memory, fed by the
+//    same TMA stages laid out in pairs.
 //  - Scores are kept in base 2: t = (q.k) * log2(e)/sqrt(D), p = 2^(t - m).
 //    The workspace m is converted back to natural units of s.
 //  - Every mbarrier wait is bounded (2 s of wall time); on timeout the kernel
@@ -40,6 +41,7 @@
 
 #include <atomic>
 
+#include "../../include/fd.h"
 #include "fd_device.cuh"
 #include "fd_internal.h"
 
@@ -168,12 +170,27 @@ struct Geo {
     static constexpr bool kF8 = KIND >= 20 && !kUmma;
     static constexpr int kWarps = KIND == 21 ? kConsumerWarpsF8 : kUmma ? 8 : kConsumerWarps;
     static constexpr int kSub = kUmma ? 64 : 16 * kWarps;      // tokens per stage
-    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : KIND == 31 ? 5 : KIND == 32 ? 4 : kStages;
+    static constexpr int kRing = KIND == 21 ? 4 : KIND == 22 ? 6 : kUmma ? 6 : kStages;
     static constexpr int kTile = kSub * 128;                   // one box of 128-byte rows
     static constexpr int kStageBytes = (kF8 ? 2 : 4) * kTile;
-    static constexpr int kOffExtra = kRing * kStageBytes;      // tcgen05: Q tile (and P, KIND 32)
-    // + the softmax exchange and the tcgen05 barriers (4 KB)
-    static constexpr int kExtraBytes = KIND == 31 ? 2 * 16384 + 4096 : KIND == 32 ? 4 * 16384 + 4096 : 0;
+    // tcgen05: consecutive stages land side by side in pairs, so that one MMA
+    // spans 128 tokens -- pair p holds four 16 KB regions (K low half, K high
+    // half, V low, V high), each [128 tokens x 64 dims]; stage 2p writes rows
+    // 0-63 of each region and stage 2p + 1 rows 64-127
+    static constexpr bool kPairs = kUmma;
+    static constexpr int kBoxStride = kPairs ? 2 * kTile : kTile;   // K lo -> K hi -> V lo -> V hi
+    static __device__ __forceinline__ uint32_t stage_off(int st) {
+        return kPairs ? static_cast<uint32_t>((st >> 1) * 4 * kBoxStride + (st & 1) * kTile)
+                      : static_cast<uint32_t>(st * kStageBytes);
+    }
+    static constexpr int kOffExtra = kRing * kStageBytes;
+    // tcgen05: KIND 32's exchange of O's lo rows (17 KB), then the softmax
+    // exchange and the tcgen05 barriers (4 KB)
+    static constexpr int kOloBytes = KIND == 32 ? 64 * 68 * 4 : 0;
+    // + the epilogue's per-warp staging of states ([16][36] floats; KIND 32
+    // writes with its four hi-side warps)
+    static constexpr int kStgBytes = KIND == 31 ? 8 * 16 * 36 * 4 : KIND == 32 ? 4 * 16 * 36 * 4 : 0;
+    static constexpr int kExtraBytes = kUmma ? kOloBytes + kStgBytes + 4096 : 0;
     static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing]
     static constexpr bool kOwnMap = kF8 || kUmma;
     static_assert(!kUmma || kSub == fdk::kSub, "the tcgen05 variant streams the 16-bit stages");
@@ -253,8 +270,9 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
         if (*c.abort_flag) break;
         const int page = page_next;
         const int tok = c.tok0 + i * kSub;
-        const uint32_t dst = smem_u32(c.smem + st * kStageBytes);
+        const uint32_t dst = smem_u32(c.smem) + Gm::stage_off(st);
         const uint32_t bar = c.full_bar(st);
+        constexpr uint32_t kBox = Gm::kBoxStride;
         if (i < first) {
             if (paged) page_next = page_of(i + 1);
             continue;
@@ -271,18 +289,18 @@ __device__ __forceinline__ void produce(const SplitCtx& c, const CUtensorMap* tm
             }
         } else if (!paged) {
             if (lane == 0) {
-                tma_load_4d_hint(dst + 0 * kHalfBytes, tmK, bar, 0, tok, c.kvh, c.b, policy);
-                tma_load_4d_hint(dst + 1 * kHalfBytes, tmK, bar, 64, tok, c.kvh, c.b, policy);
-                tma_load_4d_hint(dst + 2 * kHalfBytes, tmV, bar, 0, tok, c.kvh, c.b, policy);
-                tma_load_4d_hint(dst + 3 * kHalfBytes, tmV, bar, 64, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 0 * kBox, tmK, bar, 0, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 1 * kBox, tmK, bar, 64, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 2 * kBox, tmV, bar, 0, tok, c.kvh, c.b, policy);
+                tma_load_4d_hint(dst + 3 * kBox, tmV, bar, 64, tok, c.kvh, c.b, policy);
             }
         } else if (lane < nbox) {
             const int in_page = (tok + lane * rows) & (p.page_size - 1);
             const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
-            tma_load_4d_hint(dst + 0 * kHalfBytes + off, tmK, bar, 0, in_page, c.kvh, page, policy);
-            tma_load_4d_hint(dst + 1 * kHalfBytes + off, tmK, bar, 64, in_page, c.kvh, page, policy);
-            tma_load_4d_hint(dst + 2 * kHalfBytes + off, tmV, bar, 0, in_page, c.kvh, page, policy);
-            tma_load_4d_hint(dst + 3 * kHalfBytes + off, tmV, bar, 64, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 0 * kBox + off, tmK, bar, 0, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 1 * kBox + off, tmK, bar, 64, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 2 * kBox + off, tmV, bar, 0, in_page, c.kvh, page, policy);
+            tma_load_4d_hint(dst + 3 * kBox + off, tmV, bar, 64, in_page, c.kvh, page, policy);
         }
         issued = i + 1;
         if (paged) page_next = page_of(i + 1);   // block-table read overlaps the next wait
@@ -1056,27 +1074,46 @@ template <typename T> struct Consumer<T, 18> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 8>(c, w, l); }
 };
 
-// The start every split kernel shares: the context, the ring's barriers, the
-// programmatic-dependent-launch wait, and the split's token range.
+// The token range of split `split` of sequence b (KV head kvh): the sequence
+// cut into S balanced ranges of whole 16-token units (8 for 8-token pages), so
+// no TMA box straddles a page and a paged cache splits exactly like a
+// contiguous one.  `report`: this thread records an out-of-range length.
 template <int KIND>
-__device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const SplitParams& p,
+__device__ __forceinline__ void split_range(SplitCtx& c, int b, int kvh, int split, bool report) {
+    const SplitParams& p = *c.p;
+    c.b = b;
+    c.kvh = kvh;
+    c.split = split;
+    int L = __ldg(p.seqlens + b);
+    if (L < 0 || L > p.capacity) {
+        if (report) raise_status(kStatusSeqlenBit);
+        L = L < 0 ? 0 : p.capacity;
+    }
+    c.L = L;
+    const int S = p.n_splits;
+    const int unit = p.split_unit;
+    const int n_units = (L + unit - 1) / unit;
+    const int base = n_units / S, rem = n_units % S;
+    const int u_begin = split * base + (split < rem ? split : rem);
+    const int u_count = base + (split < rem ? 1 : 0);
+    c.tok0 = u_begin * unit;
+    c.tok1 = min((u_begin + u_count) * unit, L);
+    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Geo<KIND>::kSub - 1) / Geo<KIND>::kSub : 0;
+}
+
+// The start every split kernel shares: the context, the ring's barriers and
+// the programmatic-dependent-launch wait.
+template <int KIND>
+__device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const SplitParams& p,
                                             const CUtensorMap* tmK, const CUtensorMap* tmV) {
     using Gm = Geo<KIND>;
     constexpr int kRing = Gm::kRing;
     c.stages = kRing;
     c.p = &p;
     c.smem = smem;
-    // grid (n_splits * col_blocks, n_kv_heads, batch): the column blocks of
-    // one split are adjacent, so they run together and the later readers of
-    // the split's K/V find it in L2
-    c.split = blockIdx.x / p.col_blocks;
-    c.cb = blockIdx.x % p.col_blocks;
-    c.kvh = blockIdx.y;
-    c.b = blockIdx.z;
+    c.cb = 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int S = p.n_splits;
-
     c.bar0 = smem_u32(smem + Gm::kOffBars);
     c.abort_flag = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag);
     c.cons_abort = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 4);
@@ -1088,6 +1125,7 @@ __device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const Sp
         }
         *c.abort_flag = 0;
         *c.cons_abort = 0;
+        *reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 8) = 0;   // the tcgen05 softmax's own flag
         fence_barrier_init();
     }
     if (warp == Gm::kWarps && lane == 0) {
@@ -1099,24 +1137,18 @@ __device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const Sp
     // to finish (and its writes to land) before reading any input.
     grid_dependency_trigger();
     grid_dependency_wait();
+}
 
-    // ---- this split's token range: the sequence cut into S balanced ranges
-    // of whole 16-token units (8 for 8-token pages), so no TMA box straddles
-    // a page and a paged cache splits exactly like a contiguous one
-    int L = __ldg(p.seqlens + c.b);
-    if (L < 0 || L > p.capacity) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_status(kStatusSeqlenBit);
-        L = L < 0 ? 0 : p.capacity;
-    }
-    c.L = L;
-    const int unit = p.split_unit;
-    const int n_units = (L + unit - 1) / unit;
-    const int base = n_units / S, rem = n_units % S;
-    const int u_begin = c.split * base + (c.split < rem ? c.split : rem);
-    const int u_count = base + (c.split < rem ? 1 : 0);
-    c.tok0 = u_begin * unit;
-    c.tok1 = min((u_begin + u_count) * unit, L);
-    c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Gm::kSub - 1) / Gm::kSub : 0;
+// split_setup and the token range of the CTA's split: grid (n_splits *
+// col_blocks, n_kv_heads, batch), the column blocks of one split adjacent, so
+// they run together and the later readers of the split's K/V find it in L2.
+template <int KIND>
+__device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const SplitParams& p,
+                                            const CUtensorMap* tmK, const CUtensorMap* tmV) {
+    split_setup<KIND>(c, smem, p, tmK, tmV);
+    split_range<KIND>(c, blockIdx.z, blockIdx.y, blockIdx.x / p.col_blocks,
+                      threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0);
+    c.cb = blockIdx.x % p.col_blocks;
 }
 
 template <typename T, int KIND>
@@ -1195,492 +1227,331 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     }
 }
 
-// ---------------------------------------------------------------------------
-// tcgen05 variant (KIND 31) for query blocks of 65-128 columns (16-bit
-// caches; KIND 32 below takes 17-64): one CTA serves all G * q_len
-// (position, head) columns of a KV head as the M rows of 5th-generation
-// tensor-core MMAs with the accumulators in tensor memory, instead of one CTA
-// per 16 columns each repeating the split's arithmetic on warp MMAs.
-//   S[col][tok]  = Q[col][:] . K[tok][:]        M = 128 columns, N = 64 tokens, K = 128 dims
-//   O[col][dim] += P[col][tok] . V[tok][dim]    M = 128, N = 128 dims, K = 64 tokens (V read MN-major)
-// Q (K-major, 128-byte swizzle) is staged once in shared memory; K and V come
-// from the TMA ring exactly as for the 16-bit consumer.  P never leaves the
-// tensor memory: the softmax stores it there (hi + lo 16-bit parts, two per
-// 32-bit column) and PV takes it as its A operand.  Tensor memory holds two S
-// buffers and two P buffers (64 columns each) and O (128 columns), so the
-// softmax of stage i + 1 overlaps PV of stage i.
-// Warps 0-7 run the online softmax (base 2): warp w reaches tensor-memory
-// lanes 32 (w % 4) .. +31, i.e. columns 32 (w % 4) .. +31, and takes tokens
-// 32 (w / 4) .. +31 of each stage, so the two warps of a lane quarter split a
-// stage's tokens and exchange their maxima through shared memory.  Warp 8 is
-// the TMA producer; one thread of warp 9 issues every MMA.  A column's running
-// max moves only when a stage's max exceeds it by more than 8 (log2 units),
-// so p stays below 2^8 and O is rescaled in tensor memory only then.  The
-// states written at the end are the same (u, m, l) as the other consumers'.
-// Shared memory: 5-stage ring (160 KB), Q (32 KB), the softmax pairs'
-// exchange and the tcgen05 barriers (4 KB).
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(Geo<31>::kThreads, 1)
-    fd_split_umma_kernel(const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using Gm = Geo<31>;
-    constexpr int kRing = Gm::kRing;
-    constexpr int kSoftmaxThreads = Gm::kWarps * 32;   // 256
-    // S [0, 128) and P [128, 256) double-buffered by stage parity, O [256, 384)
-    constexpr uint32_t kTmemCols = 512;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SplitCtx c;
-    split_begin<31>(c, smem, p, &tmK, &tmV);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+// Work item `item` of the tcgen05 kernel: split item % S of KV head
+// (item / S) % n_kv_heads of sequence item / (S n_kv_heads) -- the order of
+// the other split kernels' grid.
+template <int KIND>
+__device__ __forceinline__ void set_item(SplitCtx& c, int item, bool report) {
+    const SplitParams& p = *c.p;
     const int S = p.n_splits;
-    const int n_sub = c.n_sub;
-    uint8_t* sQ = smem + Gm::kOffExtra;       // two halves [128 x 64 dims]
-    // the softmax pairs' exchange: stage maxima [stage parity][token half][column],
-    // final sums [token half][column]
-    float* xmax = reinterpret_cast<float*>(sQ + 2 * 16384);
-    float* xsum = xmax + 512;
-    // mbarriers, each [2] by stage parity except drain and the pairs'
-    const uint32_t b_pair0 = smem_u32(xsum + 256);   // [4], one per lane quarter: one arrival per warp of the pair
-    const uint32_t b_s_full = b_pair0 + 32;   // one arrival (MMA commit): S written
-    const uint32_t b_p_full = b_pair0 + 64;   // one arrival per softmax warp: P written (and O rescaled)
-    const uint32_t b_o_done = b_pair0 + 80;   // one arrival (MMA commit): PV done
-    const uint32_t b_drain = b_pair0 + 96;    // one arrival (MMA commit): every MMA done
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(xsum + 256 + 26);   // b_pair0 + 104
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) mbar_init(b_pair0 + 8u * q, 2);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(b_s_full + 8u * b, 1);
-            mbar_init(b_p_full + 8u * b, Gm::kWarps);
-            mbar_init(b_o_done + 8u * b, 1);
-        }
-        mbar_init(b_drain, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();   // every barrier is initialised
-    if (warp == Gm::kWarps) {   // the producer streams at once; Q and tensor memory follow
-        produce<31>(c, &tmK, &tmV, lane);
-        return;
-    }
-    if (threadIdx.x < 128) {
-        // Q tile: row r is column r of the group (zeros past the columns)
-        const int r = threadIdx.x;
-        bool real;
-        const T* qrow = q_row<T>(c, r, real);
-        const uint4* src = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 4
-        for (int ch = 0; ch < 16; ++ch) {
-            const uint4 v = real ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-    }
-    if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
-    tc_fence_before();
-    named_sync(3, kSoftmaxThreads + 32);   // the softmax warps and the MMA warp
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_p = tmem + 128;
-    const uint32_t tmem_o = tmem + 256;
-
-    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-
-    if (warp == Gm::kWarps + 1) {
-        // ---- MMA issue: S of stage i + 1 goes out before PV of stage i, so
-        // the softmax of one stage overlaps the tensor cores' work on the next
-        // Buffer reuse needs no waits of its own: S of stage i + 1 overwrites
-        // the scores of stage i - 1, which the softmax read before it handed
-        // over P of stage i - 1 (waited for before PV of stage i - 1); and the
-        // commit that signals S of stage i completes only after every earlier
-        // MMA, PV of stage i - 2 included, so the softmax may then overwrite
-        // that stage's P buffer.
-        if (lane == 0) {
-            // Issue cost bounds this thread: each descriptor is built once and
-            // offset by constants (the start address is the low field, in
-            // 16-byte units, and no operand crosses 256 KB, so adding never carries).
-            const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
-            const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
-            const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dk0 = umma_desc_sw128(smem_u32(c.smem), 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(smem_u32(c.smem + 2 * kHalfBytes), static_cast<uint32_t>(kHalfBytes), 1024);
-            constexpr uint32_t kStageUnits = Gm::kStageBytes >> 4;
-            auto issue_s = [&](int i) {
-                const uint64_t dk = dk0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
-                const uint32_t d = tmem + 64u * static_cast<uint32_t>(i & 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA: 32 bytes inside a 128-byte row
-                    const uint32_t q_off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
-                    const uint32_t k_off = ((kk >> 2) * static_cast<uint32_t>(kHalfBytes) + (kk & 3) * 32u) >> 4;
-                    umma_f16(d, dq + q_off, dk + k_off, id_s, kk > 0);
-                }
-                umma_commit(b_s_full + 8u * static_cast<uint32_t>(i & 1));
-            };
-            bool ok = true;
-            if (n_sub > 0) {
-                ok = wait_or_flag(c.full_bar(0), 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                }
-            }
-            for (int i = 0; ok && i < n_sub; ++i) {
-                if (i + 1 < n_sub) {
-                    const int j = i + 1;
-                    ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(j);
-                }
-                ok = wait_or_flag(b_p_full + 8u * (i & 1), (i >> 1) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t dv = dv0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
-                const uint32_t pa = tmem_p + 64u * static_cast<uint32_t>(i & 1);
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {   // P hi, then P lo
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {     // 16 tokens (two 8-row groups) per MMA
-                        // tokens 16 kk .. +15 were written by the warps of token half kk / 2:
-                        // hi at columns 32 (kk / 2) + 8 (kk % 2), lo 16 columns further
-                        const uint32_t a = pa + 32u * (kk >> 1) + 16u * part + 8u * (kk & 1);
-                        umma_f16_ta(tmem_o, a, dv + ((kk * 2048u) >> 4), id_o, i > 0 || part > 0 || kk > 0);
-                    }
-                }
-                umma_commit(b_o_done + 8u * static_cast<uint32_t>(i & 1));
-                umma_commit(c.empty_bar(i % kRing));
-            }
-            if (!ok) {
-                *c.cons_abort = 1;
-                *c.abort_flag = 1;
-            }
-            umma_commit(b_drain);              // tensor memory is freed only after this
-            wait_or_flag(b_drain, 0);
-        }
-        __syncwarp();
-    } else {
-        // ---- softmax warps: thread (w, lane) owns column r = 32 (w % 4) + lane
-        // (tensor-memory lane r) and tokens 32 h .. 32 h + 31 of each stage, h = w / 4
-        const int quarter = warp & 3, h = warp >> 2;
-        const int r = quarter * 32 + lane;
-        const bool quarter_active = quarter * 32 < p.cols;   // the pair's columns hold queries
-        const bool real = r < p.cols;
-        const int vis = real ? c.L - p.q_len + 1 + r / p.group : c.L;
-        // scores stay raw until the exponent: sc (log2(e) / sqrt(d), a 16-bit
-        // cache) is positive, so maxima of raw scores scale to maxima of scaled ones
-        const float sc = p.score_scale_log2;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t b_pair = b_pair0 + 8u * quarter;   // warps quarter and quarter + 4
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int i = 0; i < n_sub; ++i) {
-            const int buf = i & 1;
-            ok = __all_sync(kFull, wait_or_flag(b_s_full + 8u * buf, (i >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            float t[32];
-            if (quarter_active) {
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + lane_base + 64u * buf + 32u * h + 16u * q, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) t[16 * q + e] = __uint_as_float(v[e]);
-                }
-            }
-            const int tok = c.tok0 + i * Gm::kSub;
-            const int nvalid = min(Gm::kSub, c.tok1 - tok);
-            const bool partial = nvalid < Gm::kSub;
-            float alpha = 1.f;
-            bool need = false;
-            uint32_t hi[16], lo[16];
-            if (quarter_active) {
-                if (partial || tok + Gm::kSub > c.L - p.q_len + 1) {
-                    const int lim = min(nvalid, vis - tok) - 32 * h;   // in this warp's tokens
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (e >= lim) t[e] = -INFINITY;
-                }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, t[e]);
-                // the stage's max over both token halves, identical in both warps
-                // (double-buffered by stage parity: the partner has read the
-                // previous use of a slot before this warp passes the next exchange)
-                float* xm = xmax + (i & 1) * 256;
-                xm[h * 128 + r] = mx;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_pair);
-                ok = __all_sync(kFull, wait_or_flag(b_pair, i & 1));
-                if (!ok) break;
-                mx = fmaxf(mx, xm[(h ^ 1) * 128 + r]) * sc;   // raw scores: sc > 0 keeps the max
-                need = mx > m_run + 8.f;       // also true for the first finite max
-                if (need) {
-                    alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
-                    l_run *= alpha;
-                    m_run = mx;
-                }
-                const float mu = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(t[2 * e], sc, -mu));
-                    const float p1 = fast_exp2(fmaf(t[2 * e + 1], sc, -mu));
-                    l_run += p0 + p1;
-                    float k0, k1, d0, d1;
-                    hi[e] = Mma<T>::pack(p0, p1, k0, k1);
-                    lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
-                }
-            }
-            if (quarter_active) {
-                // this warp's 32 tokens: hi in its first 16 columns, lo in the next 16
-                const uint32_t pa = tmem_p + lane_base + 64u * buf + 32u * h;
-                tmem_st16(pa, hi);
-                tmem_st16(pa + 16u, lo);
-            }
-            if (i > 0 && quarter_active && __any_sync(kFull, need)) {
-                // O is rescaled once PV of stage i - 1 is done with it
-                const bool done = __all_sync(kFull, wait_or_flag(b_o_done + 8u * (buf ^ 1), ((i - 1) >> 1) & 1));
-                if (done) {
-                    tc_fence_after();
-                    // this warp's half of the column's O row
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t v[16];
-                        const uint32_t ta = tmem_o + lane_base + 64u * h + 16u * q;
-                        tmem_ld16(ta, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                        tmem_st16(ta, v);
-                    }
-                }
-                ok = done;
-            }
-            tmem_wait_st();
-            if (!ok) break;
-            if (partial) {
-                // V rows past the end hold whatever the cache holds there; P is 0
-                // for them, but 0 * NaN would still poison PV
-                uint8_t* vb = c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes;
-                for (int idx = threadIdx.x; idx < (Gm::kSub - nvalid) * 16; idx += kSoftmaxThreads) {
-                    const int row = nvalid + (idx >> 4), ch = idx & 15;
-                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + row * 128 + ((ch & 7) << 4)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_p_full + 8u * buf);
-        }
-        if (ok && n_sub > 0) {   // the last PV done (it completes after every earlier one)
-            ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * ((n_sub - 1) & 1), ((n_sub - 1) >> 1) & 1));
-            tc_fence_after();
-        }
-        if (!ok) *c.cons_abort = 1;
-        xsum[h * 128 + r] = l_run;
-        named_sync(1, kSoftmaxThreads);
-        if (*c.cons_abort == 0 && quarter_active) {
-            // the column's state (u, m, l), or out / lse directly with one split;
-            // this warp writes dims 64 h .. 64 h + 63
-            const float l_col = xsum[r] + xsum[128 + r];
-            const int64_t row = real ? (static_cast<int64_t>(c.b) * p.q_len + r / p.group) * p.n_q_heads +
-                                           c.kvh * p.group + r % p.group
-                                     : 0;
-            const float m_out = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
-            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t v[16];
-                if (n_sub > 0) {
-                    tmem_ld16(tmem_o + lane_base + 64u * h + 16u * q, v);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = 0u;
-                }
-                if (!real) continue;
-                const int d0 = 64 * h + 16 * q;
-                if (p.direct) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float o = empty ? 0.f : (__uint_as_float(v[e]) * p.v_scale) / l_col;
-                        const int64_t oi = row * kHeadDim + d0 + e;
-                        if (p.out_dtype == 2)
-                            static_cast<float*>(p.out)[oi] = o;
-                        else if (p.out_dtype == 0)
-                            static_cast<__half*>(p.out)[oi] = __float2half_rn(o);
-                        else
-                            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.ws_u + (row * S + c.split) * kHeadDim + d0);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_float4(__uint_as_float(v[4 * e]) * p.v_scale, __uint_as_float(v[4 * e + 1]) * p.v_scale,
-                                             __uint_as_float(v[4 * e + 2]) * p.v_scale, __uint_as_float(v[4 * e + 3]) * p.v_scale);
-                }
-            }
-            if (real && h == 0) {
-                if (p.direct) {
-                    if (p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l_col);
-                } else {
-                    p.ws_m[row * S + c.split] = m_out;
-                    p.ws_l[row * S + c.split] = l_col;
-                }
-            }
-        }
-    }
-    // every tensor-memory user is done (the MMA thread waited for its last commit)
-    tc_fence_before();
-    named_sync(2, kSoftmaxThreads + 32);
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    const int rest = item / S;
+    split_range<KIND>(c, rest / p.n_kv_heads, rest % p.n_kv_heads, item - rest * S, report);
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 variant for 17-64 columns (KIND 32).  Every tcgen05.mma costs the
-// tensor pipe about the same time up to N = 128, so this variant fills the
-// M = 128 rows twice over instead of leaving half of them empty:
-//   Q rows 64 + c repeat rows c, so S lanes 64 + c repeat the scores of column c;
-//   P rows 0..63 hold the hi parts of the columns' weights, rows 64..127 the lo parts,
-//   and one MMA per 16 tokens accumulates O rows c (hi) and 64 + c (lo) together.
-// PV takes 4 MMAs per stage instead of 8, and the result is O[c] = O[c] + O[64 + c]
-// at the end.  Each column is served by four softmax warps (both lane quarters
-// that hold its scores, two warps each), each taking 16 of a stage's 64 tokens;
-// the four exchange their maxima every stage, so all four track the same
-// running max and each rescales its own O rows when it moves.  P is written to
-// shared memory (K-major, 128-byte swizzle), double-buffered by stage parity.
-// Shared memory: 4-stage ring (128 KB), Q (32 KB), P (2 x 16 KB), the
-// exchange and the tcgen05 barriers (4 KB).
+// Producer of the tcgen05 kernel: streams the stages of every work item
+// (split) the CTA serves, back to back, into the ring in pairs of slots.  An
+// item with an odd number of stages leaves the second slot of its last pair
+// unfilled (its full barrier gets a plain arrival), so every pair starts on an
+// even slot and each slot's barrier phases stay in step.
 // ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(Geo<32>::kThreads, 1)
-    fd_split_umma64_kernel(const __grid_constant__ CUtensorMap tmK,
-                           const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using Gm = Geo<32>;
+template <int KIND>
+__device__ __forceinline__ void produce_pairs(const SplitCtx& c0, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, int lane, int n_items) {
+    using Gm = Geo<KIND>;
     constexpr int kRing = Gm::kRing;
+    constexpr uint32_t kBox = Gm::kBoxStride;
+    const SplitParams& p = *c0.p;
+    const uint64_t policy = policy_evict_first();   // K/V are read once
+    const bool paged = p.page_size != 0;
+    const int rows = paged ? min(kPagedBoxRows, p.page_size) : kSub;   // tokens per box
+    const int nbox = kSub / rows;                                        // boxes per half per stage
+    const int first = p.drop_first_stage ? 1 : 0;   // test hook: slot 0 is never filled
+    int gs = 0;                                     // slots used so far, over all items
+    bool stop = false;
+    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+        SplitCtx c = c0;
+        set_item<KIND>(c, item, false);
+        const int n_slots = 2 * ((c.n_sub + 1) >> 1);
+        // physical page of box `lane` of stage i (paged); -1 reads zeros
+        auto page_of = [&](int i) -> int {
+            const int t = c.tok0 + i * kSub + lane * rows;
+            if (lane >= nbox || i >= c.n_sub || t >= c.tok1) return -1;
+            const int pg = __ldg(p.block_table + static_cast<size_t>(c.b) * p.max_pages +
+                                 (t >> p.page_shift));
+            if (pg < 0 || pg >= p.n_pages) {
+                raise_status(kStatusPageBit);
+                return -1;
+            }
+            return pg;
+        };
+        int page_next = paged ? page_of(0) : 0;
+#pragma unroll 1
+        for (int i = 0; i < n_slots; ++i, ++gs) {
+            const int st = gs % kRing;
+            if (gs >= kRing) {
+                const bool ok = wait_or_flag(c.empty_bar(st), ((gs / kRing) - 1) & 1);
+                if (!__all_sync(kFull, ok)) *c.abort_flag = 1;
+            }
+            if (*c.abort_flag) {
+                stop = true;
+                break;
+            }
+            const int page = page_next;
+            if (paged) page_next = page_of(i + 1);
+            if (gs < first) continue;
+            const uint32_t bar = c.full_bar(st);
+            if (i >= c.n_sub) {   // the unfilled half of an odd item's last pair
+                if (lane == 0) mbar_arrive(bar);
+                __syncwarp();
+                continue;
+            }
+            const int tok = c.tok0 + i * kSub;
+            const uint32_t dst = smem_u32(c.smem) + Gm::stage_off(st);
+            if (lane == 0) mbar_arrive_expect_tx(bar, Gm::kStageBytes);
+            __syncwarp();
+            if (!paged) {
+                if (lane == 0) {
+                    tma_load_4d_hint(dst + 0 * kBox, tmK, bar, 0, tok, c.kvh, c.b, policy);
+                    tma_load_4d_hint(dst + 1 * kBox, tmK, bar, 64, tok, c.kvh, c.b, policy);
+                    tma_load_4d_hint(dst + 2 * kBox, tmV, bar, 0, tok, c.kvh, c.b, policy);
+                    tma_load_4d_hint(dst + 3 * kBox, tmV, bar, 64, tok, c.kvh, c.b, policy);
+                }
+            } else if (lane < nbox) {
+                const int in_page = (tok + lane * rows) & (p.page_size - 1);
+                const uint32_t off = static_cast<uint32_t>(lane * rows * 128);
+                tma_load_4d_hint(dst + 0 * kBox + off, tmK, bar, 0, in_page, c.kvh, page, policy);
+                tma_load_4d_hint(dst + 1 * kBox + off, tmK, bar, 64, in_page, c.kvh, page, policy);
+                tma_load_4d_hint(dst + 2 * kBox + off, tmV, bar, 0, in_page, c.kvh, page, policy);
+                tma_load_4d_hint(dst + 3 * kBox + off, tmV, bar, 64, in_page, c.kvh, page, policy);
+            }
+        }
+    }
+    // Drain: the last fill of each slot must have landed before this CTA may
+    // exit (a no-op unless a consumer gave up).
+    if (lane == 0) {
+        for (int g = max(first, gs - kRing); g < gs; ++g) wait_or_flag(c0.full_bar(g % kRing), (g / kRing) & 1);
+    }
+}
+
+// Walks the pairs of stages of a persistent CTA's items in order, skipping
+// items with no keys; kq counts the non-empty items before the current one.
+template <int KIND>
+struct PairWalk {
+    SplitCtx c;        // the current item's range
+    int item, n_items;
+    int j, n_pairs, kq;
+    bool done;
+
+    __device__ __forceinline__ void seek() {   // from `item` on, the first non-empty item
+        for (; item < n_items; item += gridDim.x) {
+            set_item<KIND>(c, item, false);
+            n_pairs = (c.n_sub + 1) >> 1;
+            if (n_pairs > 0) return;
+        }
+        done = true;
+    }
+    __device__ __forceinline__ void start(const SplitCtx& c0, int n) {
+        c = c0;
+        item = blockIdx.x;
+        n_items = n;
+        j = 0;
+        kq = 0;
+        done = false;
+        seek();
+    }
+    __device__ __forceinline__ void next() {
+        if (++j < n_pairs) return;
+        j = 0;
+        ++kq;
+        item += gridDim.x;
+        seek();
+    }
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 kernel for query blocks of 17-128 columns (16-bit caches): one CTA
+// serves all G * q_len (position, head) columns of a KV head as the M rows of
+// 5th-generation tensor-core MMAs with the accumulators in tensor memory,
+// instead of one CTA per 16 columns each repeating the split's arithmetic on
+// warp MMAs.  Per pair of 64-token stages (128 tokens, side by side in shared
+// memory, see Geo):
+//   S[col][tok]  = Q[col][:] . K[tok][:]        M = 128, N = 128 tokens, K = 128 dims (8 MMAs)
+//   O[col][dim] += P[col][tok] . V[tok][dim]    M = 128, N = 128 dims, 16 tokens per MMA
+// A tcgen05.mma costs its issuing thread about the same time whatever N up to
+// 128, so S over a whole pair (N = 128) halves the S MMAs of 64-token stages.
+// Q is staged into tensor memory (the A operand of S); P (hi + lo 16-bit parts
+// of the weights, two per 32-bit column) is written by the softmax over the
+// columns that held its scores and read by PV as its A operand.  The next S
+// into that buffer is issued after PV, and tcgen05 MMAs of one thread run in
+// issue order, so PV has read P before S overwrites it.
+//   KIND 31 (65-128 columns): lane r is column r; PV takes P's hi and lo
+//     parts as two MMAs per 16 tokens (16 per pair).
+//   KIND 32 (17-64 columns): Q rows 64 + c repeat rows c, so lanes 64 + c
+//     hold column c's scores again; lanes 0-63 of P hold the hi parts and
+//     lanes 64-127 the lo parts, so one MMA per 16 tokens accumulates both
+//     (8 per pair), and O[c] + O[64 + c] is the result.
+// Persistent: the grid is one CTA per SM (or per work item if fewer), and CTA
+// c serves the work items (split, KV head, sequence) c, c + gridDim.x, ...
+// back to back -- the producer streams the next item's stages without a
+// break, the next item's Q goes to the second Q buffer while the current item
+// runs, and an item's epilogue (O read out, state written) overlaps the next
+// item's first S MMAs; PV of the next item waits for it to release O.
+// Warps 0-7 run the online softmax (base 2): warp w reaches tensor-memory
+// lanes 32 (w % 4) .. +31 and takes tokens 64 (w / 4) .. +63 of each pair;
+// the warps that share a column exchange their maxima once per pair (two
+// warps, or four for KIND 32, whose hi and lo lanes must move their maxima
+// together).  Warp 8 is the TMA producer; one thread of warp 9 issues every
+// MMA.  A column's running max moves only when a pair's max exceeds it by
+// more than 8 (log2 units), so p stays below 2^8 and O is rescaled in tensor
+// memory only then.  The states written are the same (u, m, l) as the other
+// consumers'.
+// Tensor memory (512 columns): S/P [0, 128) and [128, 256) by pair parity,
+// O [256, 384), Q [384, 448) and [448, 512) by item parity.  Shared memory:
+// the 3-pair ring (192 KB), KIND 32's exchange of O's lo rows (17 KB), the
+// epilogue's per-warp staging of states (2.3 KB a warp), the
+// softmax exchange and the tcgen05 barriers (4 KB).
+// ---------------------------------------------------------------------------
+template <typename T, int KIND>
+__global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
+    fd_split_umma_kernel(const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using Gm = Geo<KIND>;
+    constexpr bool kStack = KIND == 32;
+    constexpr int kRing = Gm::kRing;
+    constexpr int kPairSlots = kRing / 2;
     constexpr int kSoftmaxThreads = Gm::kWarps * 32;   // 256
-    constexpr uint32_t kTmemCols = 256;       // S [0, 128) double-buffered by stage parity, O [128, 256)
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kColO = 256, kColQ = 384;
+    constexpr uint32_t kRegion = Gm::kBoxStride;       // 16 KB: [128 tokens x 64 dims]
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     SplitCtx c;
-    split_begin<32>(c, smem, p, &tmK, &tmV);
+    split_setup<KIND>(c, smem, p, &tmK, &tmV);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
-    const int n_sub = c.n_sub;
-    uint8_t* sQ = smem + Gm::kOffExtra;       // two halves [128 x 64 dims]
-    uint8_t* sP = sQ + 2 * 16384;             // [stage parity][128 rows x 64 tokens]
-    // the exchange: stage maxima [stage parity][token quarter][column], sums [token quarter][column]
-    float* xmax = reinterpret_cast<float*>(sP + 2 * 16384);
+    const int n_items = S * p.n_kv_heads * p.batch;
+    // KIND 32: O's lo rows pass through shared memory, [64 columns][68 words] of bf16 pairs
+    uint32_t* olo_w = reinterpret_cast<uint32_t*>(smem + Gm::kOffExtra);
+    // the epilogue's staging of a warp's 16 rows x 32 dims, rows padded to 36
+    // floats (each 8-lane phase of a 16-byte access meets distinct banks)
+    constexpr int kStgRow = 36;
+    constexpr int kStgWarp = 16 * kStgRow;
+    constexpr int kOloRow = 68;   // KIND 32: words per column of the lo exchange (64 + 4 padding)
+    static_assert(!kStack || 64 * kOloRow * 4 <= Gm::kOloBytes, "the lo exchange must fit");
+    float* stg = reinterpret_cast<float*>(smem + Gm::kOffExtra + Gm::kOloBytes);
+    // the softmax exchange: pair maxima [pair parity][256], final sums [256]
+    float* xmax = reinterpret_cast<float*>(smem + Gm::kOffExtra + Gm::kOloBytes + Gm::kStgBytes);
     float* xsum = xmax + 512;
-    // mbarriers, [2] by stage parity unless noted
-    const uint32_t b_grp0 = smem_u32(xsum + 256);   // [2], one per column group: one arrival per warp of its four
-    const uint32_t b_s_full = b_grp0 + 16;    // one arrival (MMA commit): S written
-    const uint32_t b_p_full = b_grp0 + 48;    // one arrival per softmax warp: P written (and O rescaled)
-    const uint32_t b_o_done = b_grp0 + 64;    // one arrival (MMA commit): PV done
-    const uint32_t b_drain = b_grp0 + 80;     // single, one arrival (MMA commit): every MMA done
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(xsum + 256 + 22);   // b_grp0 + 88
+    // mbarriers, [2] by pair parity (q_full: by item parity) unless noted
+    const uint32_t b_x0 = smem_u32(xsum + 256);   // [4] exchange, one per group of warps sharing columns
+    const uint32_t b_s_full = b_x0 + 32;          // one arrival (MMA commit): S written
+    const uint32_t b_p_full = b_x0 + 48;          // one arrival per softmax warp: P written (and O rescaled)
+    const uint32_t b_o_done = b_x0 + 64;          // one arrival (MMA commit): PV done
+    const uint32_t b_q_full = b_x0 + 80;          // one arrival per softmax warp: an item's Q staged
+    const uint32_t b_o_free = b_x0 + 96;          // single, one arrival per softmax warp: O read out
+    const uint32_t b_drain = b_x0 + 104;          // single, one arrival (MMA commit): every MMA done
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(xsum + 256 + 28);   // b_x0 + 112
     if (threadIdx.x == 0) {
 #pragma unroll
+        for (int g = 0; g < 4; ++g) mbar_init(b_x0 + 8u * g, kStack ? 4 : 2);
+#pragma unroll
         for (int b = 0; b < 2; ++b) {
-            mbar_init(b_grp0 + 8u * b, 4);
             mbar_init(b_s_full + 8u * b, 1);
             mbar_init(b_p_full + 8u * b, Gm::kWarps);
             mbar_init(b_o_done + 8u * b, 1);
+            mbar_init(b_q_full + 8u * b, Gm::kWarps);
         }
+        mbar_init(b_o_free, Gm::kWarps);
         mbar_init(b_drain, 1);
         fence_barrier_init();
     }
     __syncthreads();   // every barrier is initialised
     if (warp == Gm::kWarps) {   // the producer streams at once; Q and tensor memory follow
-        produce<32>(c, &tmK, &tmV, lane);
+        produce_pairs<KIND>(c, &tmK, &tmV, lane, n_items);
         return;
-    }
-    if (threadIdx.x < 128) {
-        // Q tile: rows r and 64 + r are column r of the group (zeros past the columns)
-        const int r = threadIdx.x;
-        bool real;
-        const T* qrow = q_row<T>(c, r & 63, real);
-        const uint4* src = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 4
-        for (int ch = 0; ch < 16; ++ch) {
-            const uint4 v = real ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sQ + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
     }
     if (warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tc_fence_before();
     named_sync(3, kSoftmaxThreads + 32);   // the softmax warps and the MMA warp
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 128;
+    const uint32_t tmem_o = tmem + kColO;
 
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
 
     if (warp == Gm::kWarps + 1) {
-        // ---- MMA issue (one thread): S of stage i + 1 goes out before PV of stage i.
-        // Each descriptor is built once and offset by constants (the start address
-        // is the low field, in 16-byte units, and no operand crosses 256 KB).
-        // Buffer reuse needs no waits of its own: S of stage i + 1 overwrites
-        // the scores of stage i - 1, which the softmax read before it handed
-        // over P of stage i - 1 (waited for before PV of stage i - 1); and the
-        // commit that signals S of stage i completes only after every earlier
-        // MMA, PV of stage i - 2 included, so the softmax may then overwrite
-        // that stage's P buffer.
+        // ---- MMA issue: S of the next pair goes out before PV of the current
+        // one, so the softmax of one pair overlaps the tensor cores' work on
+        // the next (also across items).  The scores of pair g - 1, which S of
+        // pair g + 1 overwrites, were read before the softmax handed over P of
+        // pair g - 1, which PV of pair g - 1 (issued earlier) reads first.
+        // Each descriptor is built once and offset by constants (the start
+        // address is the low field, in 16-byte units, and no operand crosses
+        // 256 KB).
         if (lane == 0) {
-            const uint32_t id_s = umma_idesc_f16(128, 64, kBf16, false);
+            const uint32_t id_s = umma_idesc_f16(128, 128, kBf16, false);
+            const uint32_t id_s64 = umma_idesc_f16(128, 64, kBf16, false);   // a pair's lone stage
             const uint32_t id_o = umma_idesc_f16(128, 128, kBf16, true);
-            const uint64_t dq = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dp0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(smem_u32(c.smem), 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(smem_u32(c.smem + 2 * kHalfBytes), static_cast<uint32_t>(kHalfBytes), 1024);
-            constexpr uint32_t kStageUnits = Gm::kStageBytes >> 4;
-            auto issue_s = [&](int i) {
-                const uint64_t dk = dk0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
-                const uint32_t d = tmem + 64u * static_cast<uint32_t>(i & 1);
+            const uint64_t dv0 = umma_desc_sw128(smem_u32(c.smem + 2 * kRegion), kRegion, 1024);
+            constexpr uint32_t kPairUnits = (4 * kRegion) >> 4;
+            // S of pair gp: the item's Q (ready), both stages landed (a last pair may have one)
+            auto issue_s = [&](const PairWalk<KIND>& w, int gp) -> bool {
+                if (w.j == 0 && !wait_or_flag(b_q_full + 8u * (w.kq & 1), (w.kq >> 1) & 1)) return false;
+                const int s0 = 2 * gp;
+                const bool two = 2 * w.j + 1 < w.c.n_sub;
+                if (!wait_or_flag(c.full_bar(s0 % kRing), (s0 / kRing) & 1)) return false;
+                if (two && !wait_or_flag(c.full_bar((s0 + 1) % kRing), ((s0 + 1) / kRing) & 1)) return false;
+                tc_fence_after();
+                const uint64_t dk = dk0 + static_cast<uint32_t>(gp % kPairSlots) * kPairUnits;
+                const uint32_t d = tmem + 128u * static_cast<uint32_t>(gp & 1);
+                const uint32_t tq = tmem + kColQ + 64u * static_cast<uint32_t>(w.kq & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {   // 16 dims per MMA: 32 bytes inside a 128-byte row
-                    const uint32_t q_off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
-                    const uint32_t k_off = ((kk >> 2) * static_cast<uint32_t>(kHalfBytes) + (kk & 3) * 32u) >> 4;
-                    umma_f16(d, dq + q_off, dk + k_off, id_s, kk > 0);
+                    const uint32_t k_off = ((kk >> 2) * kRegion + (kk & 3) * 32u) >> 4;
+                    umma_f16_ta(d, tq + 8u * kk, dk + k_off, two ? id_s : id_s64, kk > 0);
                 }
-                umma_commit(b_s_full + 8u * static_cast<uint32_t>(i & 1));
+                umma_commit(b_s_full + 8u * static_cast<uint32_t>(gp & 1));
+                return true;
             };
+            PairWalk<KIND> ws, wv;   // the pair S is issued for next, the pair PV is
+            ws.start(c, n_items);
+            wv = ws;
+            int gps = 0, gpv = 0;
             bool ok = true;
-            if (n_sub > 0) {
-                ok = wait_or_flag(c.full_bar(0), 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                }
-            }
-            for (int i = 0; ok && i < n_sub; ++i) {
-                if (i + 1 < n_sub) {
-                    const int j = i + 1;
-                    ok = wait_or_flag(c.full_bar(j % kRing), (j / kRing) & 1);
+            if (!ws.done) ok = issue_s(ws, gps);
+            while (ok && !wv.done) {
+                ws.next();
+                ++gps;
+                // at an item boundary PV of the item's last pair goes first, so that
+                // the item's epilogue can start sooner
+                const bool boundary = !ws.done && ws.j == 0;
+                if (!ws.done && !boundary) {
+                    ok = issue_s(ws, gps);
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_s(j);
                 }
-                ok = wait_or_flag(b_p_full + 8u * (i & 1), (i >> 1) & 1);
+                ok = wait_or_flag(b_p_full + 8u * (gpv & 1), (gpv >> 1) & 1);
                 if (!ok) break;
+                if (wv.j == 0 && wv.kq > 0) {   // the last item's epilogue has read O
+                    ok = wait_or_flag(b_o_free, (wv.kq - 1) & 1);
+                    if (!ok) break;
+                }
                 tc_fence_after();
-                const uint64_t dv = dv0 + static_cast<uint32_t>(i % kRing) * kStageUnits;
-                const uint64_t dp = dp0 + static_cast<uint32_t>(i & 1) * (16384u >> 4);
+                const uint64_t dv = dv0 + static_cast<uint32_t>(gpv % kPairSlots) * kPairUnits;
+                const uint32_t pa = tmem + 128u * static_cast<uint32_t>(gpv & 1);
+                const bool two = 2 * wv.j + 1 < wv.c.n_sub;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // 16 tokens per MMA: hi and lo rows together
-                    umma_f16(tmem_o, dp + ((kk * 32u) >> 4), dv + ((kk * 2048u) >> 4), id_o, i > 0 || kk > 0);
-                umma_commit(b_o_done + 8u * static_cast<uint32_t>(i & 1));
-                umma_commit(c.empty_bar(i % kRing));
+                for (int kk = 0; kk < 8; ++kk) {   // 16 tokens per MMA
+                    if (kk == 4 && !two) break;
+                    // tokens 16 kk .. +15 were written by the warps of token half kk / 4:
+                    // hi at columns 64 (kk / 4) + 8 (kk % 4), lo 32 columns further
+                    const uint32_t a = pa + 64u * (kk >> 2) + 8u * (kk & 3);
+                    const uint64_t b = dv + ((kk * 2048u) >> 4);
+                    umma_f16_ta(tmem_o, a, b, id_o, wv.j > 0 || kk > 0);
+                    if (!kStack) umma_f16_ta(tmem_o, a + 32u, b, id_o, true);
+                }
+                umma_commit(b_o_done + 8u * static_cast<uint32_t>(gpv & 1));
+                umma_commit(c.empty_bar((2 * gpv) % kRing));        // both slots, filled or not
+                umma_commit(c.empty_bar((2 * gpv + 1) % kRing));
+                wv.next();
+                ++gpv;
+                if (boundary) {
+                    ok = issue_s(ws, gps);
+                    if (!ok) break;
+                }
             }
             if (!ok) {
                 *c.cons_abort = 1;
@@ -1691,203 +1562,359 @@ __global__ void __launch_bounds__(Geo<32>::kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- softmax warps.  Warp w reaches tensor-memory lanes 32 q .. +31,
-        // q = w % 4: the scores (and O rows) of columns col = 32 (q % 2) + lane,
-        // the hi rows for q < 2 and the lo rows for q >= 2.  Its tokens are
-        // 16 tq .. 16 tq + 15 of each stage, tq = 2 (q / 2) + w / 4, and its O
-        // dims are 64 (w / 4) .. +63.  Column group g = q % 2 has the four warps
-        // g, g + 2, g + 4, g + 6.
-        const int q = warp & 3, hw = warp >> 2;
-        const int g = q & 1, side = q >> 1;
-        const int col = 32 * g + lane;
-        const int tq = 2 * side + hw;
-        const bool group_active = 32 * g < p.cols;
+        // ---- softmax warps: thread (w, lane) owns column `col` (tensor-memory
+        // lane r) and tokens 64 h .. 64 h + 63 of each pair; for KIND 32 side
+        // 0 holds the hi lanes and side 1 the lo lanes
+        const int q = warp & 3, h = (warp >> 2) & 1;
+        const int r = q * 32 + lane;
+        const int col = kStack ? (r & 63) : r;
+        const int side = kStack ? (q >> 1) : 0;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const bool active = kStack ? 32 * (q & 1) < p.cols : 32 * q < p.cols;   // warp-uniform
         const bool real = col < p.cols;
-        const int vis = real ? c.L - p.q_len + 1 + col / p.group : c.L;
         // scores stay raw until the exponent: sc (log2(e) / sqrt(d), a 16-bit
         // cache) is positive, so maxima of raw scores scale to maxima of scaled ones
         const float sc = p.score_scale_log2;
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t b_grp = b_grp0 + 8u * g;
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int i = 0; i < n_sub; ++i) {
-            const int buf = i & 1;
-            ok = __all_sync(kFull, wait_or_flag(b_s_full + 8u * buf, (i >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            float t[16];
-            if (group_active) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_base + 64u * buf + 16u * tq, v);
-                tmem_wait_ld();
+        const uint32_t b_x = b_x0 + 8u * static_cast<uint32_t>(kStack ? (q & 1) : q);
+        const int xslot = kStack ? (side * 2 + h) * 64 + col : h * 128 + r;
+        // Q of a non-empty item into buffer kb: this lane's row, dims 64 h .. +63
+        // (d, d + 1 share column d / 2); every softmax warp arrives on q_full
+        auto stage_q = [&](const SplitCtx& ci, int kb) {
+            bool rl;
+            const T* qrow = q_row<T>(ci, col, rl);
+            const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * h);
+            uint32_t qw[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) t[e] = __uint_as_float(v[e]);
+            for (int x = 0; x < 8; ++x) {
+                const uint4 v = rl ? __ldg(src + x) : make_uint4(0u, 0u, 0u, 0u);
+                qw[4 * x] = v.x;
+                qw[4 * x + 1] = v.y;
+                qw[4 * x + 2] = v.z;
+                qw[4 * x + 3] = v.w;
             }
-            const int tok = c.tok0 + i * Gm::kSub;
-            const int nvalid = min(Gm::kSub, c.tok1 - tok);
-            const bool partial = nvalid < Gm::kSub;
-            float alpha = 1.f;
-            bool need = false;
-            uint32_t hi[8], lo[8];
-            if (group_active) {
-                if (partial || tok + Gm::kSub > c.L - p.q_len + 1) {
-                    const int lim = min(nvalid, vis - tok) - 16 * tq;   // in this warp's tokens
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (e >= lim) t[e] = -INFINITY;
-                }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) mx = fmaxf(mx, t[e]);
-                // the stage's max over the four token quarters, identical in the
-                // group's four warps (double-buffered by stage parity: every warp
-                // has read a slot before the group passes its next exchange)
-                float* xm = xmax + (i & 1) * 256;
-                xm[tq * 64 + col] = mx;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_grp);
-                ok = __all_sync(kFull, wait_or_flag(b_grp, i & 1));
-                if (!ok) break;
-                mx = fmaxf(fmaxf(xm[col], xm[64 + col]), fmaxf(xm[128 + col], xm[192 + col])) * sc;
-                need = mx > m_run + 8.f;       // also true for the first finite max
-                if (need) {
-                    alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
-                    l_run *= alpha;
-                    m_run = mx;
-                }
-                const float mu = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float p0 = fast_exp2(fmaf(t[2 * e], sc, -mu));
-                    const float p1 = fast_exp2(fmaf(t[2 * e + 1], sc, -mu));
-                    l_run += p0 + p1;
-                    float k0, k1, d0, d1;
-                    hi[e] = Mma<T>::pack(p0, p1, k0, k1);
-                    lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
-                }
-            }
-            if (group_active) {
-                // tokens 16 tq .. +15 = chunks 2 tq, 2 tq + 1 of rows col (hi) and 64 + col (lo)
-                uint8_t* pb = sP + buf * 16384;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int chunk = 2 * tq + h2;
-                    const int rh = col, rl = 64 + col;
-                    *reinterpret_cast<uint4*>(pb + rh * 128 + ((chunk ^ (rh & 7)) << 4)) =
-                        make_uint4(hi[4 * h2], hi[4 * h2 + 1], hi[4 * h2 + 2], hi[4 * h2 + 3]);
-                    *reinterpret_cast<uint4*>(pb + rl * 128 + ((chunk ^ (rl & 7)) << 4)) =
-                        make_uint4(lo[4 * h2], lo[4 * h2 + 1], lo[4 * h2 + 2], lo[4 * h2 + 3]);
-                }
-            }
-            if (i > 0 && group_active && __any_sync(kFull, need)) {
-                // O is rescaled once PV of stage i - 1 is done with it: this warp's
-                // 32 O rows, dims 64 hw .. +63
-                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * (buf ^ 1), ((i - 1) >> 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int qq = 0; qq < 4; ++qq) {
-                    uint32_t v[16];
-                    const uint32_t ta = tmem_o + lane_base + 64u * hw + 16u * qq;
-                    tmem_ld16(ta, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st16(ta, v);
-                }
-                tmem_wait_st();
-            }
-            if (partial) {
-                // V rows past the end hold whatever the cache holds there; P is 0
-                // for them, but 0 * NaN would still poison PV
-                uint8_t* vb = c.smem + (i % kRing) * Gm::kStageBytes + 2 * kHalfBytes;
-                for (int idx = threadIdx.x; idx < (Gm::kSub - nvalid) * 16; idx += kSoftmaxThreads) {
-                    const int row = nvalid + (idx >> 4), ch = idx & 15;
-                    *reinterpret_cast<uint4*>(vb + (ch >> 3) * kHalfBytes + row * 128 + ((ch & 7) << 4)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            fence_proxy_async_smem();
+            const uint32_t qa = tmem + lane_base + kColQ + 64u * static_cast<uint32_t>(kb & 1) + 32u * h;
+            tmem_st16(qa, *reinterpret_cast<const uint32_t(*)[16]>(qw));
+            tmem_st16(qa + 16u, *reinterpret_cast<const uint32_t(*)[16]>(qw + 16));
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_p_full + 8u * buf);
-        }
-        if (ok && n_sub > 0) {   // the last PV done (it completes after every earlier one)
-            ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * ((n_sub - 1) & 1), ((n_sub - 1) >> 1) & 1));
-            tc_fence_after();
-        }
-        if (!ok) *c.cons_abort = 1;
-        xsum[tq * 64 + col] = l_run;
-        // the lo rows of O go through shared memory (ring stage 0, idle now):
-        // [64 columns][128 dims] fp32
-        float* olo = reinterpret_cast<float*>(c.smem);
-        if (ok && side == 1 && group_active && n_sub > 0) {
-#pragma unroll 1
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t v[16];
-                tmem_ld16(tmem_o + lane_base + 64u * hw + 16u * qq, v);
-                tmem_wait_ld();
-                float4* dst = reinterpret_cast<float4*>(olo + col * kHeadDim + 64 * hw + 16 * qq);
+            if (lane == 0) mbar_arrive(b_q_full + 8u * static_cast<uint32_t>(kb & 1));
+        };
+        // the state of an item's column: (u, m, l), or out / lse with one split;
+        // o: 16 dims d0 .. d0 + 15 of u (unscaled by v), this thread's row
+        auto write_state = [&](const SplitCtx& ci, int d0, const float (&o)[16], float m_out, float l_col,
+                               bool with_ml) {
+            const int64_t row = (static_cast<int64_t>(ci.b) * p.q_len + col / p.group) * p.n_q_heads +
+                                ci.kvh * p.group + col % p.group;
+            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
+            if (p.direct) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float y = empty ? 0.f : (o[e] * p.v_scale) / l_col;
+                    const int64_t oi = row * kHeadDim + d0 + e;
+                    if (p.out_dtype == 2)
+                        static_cast<float*>(p.out)[oi] = y;
+                    else if (p.out_dtype == 0)
+                        static_cast<__half*>(p.out)[oi] = __float2half_rn(y);
+                    else
+                        static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(y);
+                }
+                if (with_ml && p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l_col);
+            } else {
+                float4* dst = reinterpret_cast<float4*>(p.ws_u + (row * S + ci.split) * kHeadDim + d0);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                    dst[e] = make_float4(o[4 * e] * p.v_scale, o[4 * e + 1] * p.v_scale,
+                                         o[4 * e + 2] * p.v_scale, o[4 * e + 3] * p.v_scale);
+                if (with_ml) {
+                    p.ws_m[row * S + ci.split] = m_out;
+                    p.ws_l[row * S + ci.split] = l_col;
+                }
             }
-        }
-        named_sync(1, kSoftmaxThreads);
-        if (*c.cons_abort == 0 && side == 0 && group_active) {
-            // the column's state (u, m, l), or out / lse directly with one split;
-            // this warp writes dims 64 hw .. 64 hw + 63
-            const float l_col = (xsum[col] + xsum[64 + col]) + (xsum[128 + col] + xsum[192 + col]);
-            const int64_t row = real ? (static_cast<int64_t>(c.b) * p.q_len + col / p.group) * p.n_q_heads +
-                                           c.kvh * p.group + col % p.group
-                                     : 0;
-            const float m_out = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
-            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
+        };
+
+        // set by softmax warps only, read by all of them between two barriers
+        volatile int* sm_abort = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 8);
+        PairWalk<KIND> wq;   // the next non-empty item whose Q is to be staged
+        wq.start(c, n_items);
+        if (!wq.done) stage_q(wq.c, 0);
+        int gp = 0, kq = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            SplitCtx ci = c;
+            set_item<KIND>(ci, item, threadIdx.x == 0);
+            const int n_pairs = (ci.n_sub + 1) >> 1;
+            if (n_pairs == 0) {   // no keys: u = 0, m = -inf, l = 0
+                if (side == 0 && active && real) {
+                    const float zero[16] = {};
 #pragma unroll 1
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t v[16];
-                if (n_sub > 0) {
-                    tmem_ld16(tmem_o + lane_base + 64u * hw + 16u * qq, v);
+                    for (int qq = 0; qq < 4; ++qq) write_state(ci, 64 * h + 16 * qq, zero, -INFINITY, 0.f, h == 0 && qq == 0);
+                }
+                continue;
+            }
+            const int vis = real ? ci.L - p.q_len + 1 + col / p.group : ci.L;
+            float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll 1
+            for (int j = 0; j < n_pairs; ++j, ++gp) {
+                const int buf = gp & 1;
+                ok = __all_sync(kFull, wait_or_flag(b_s_full + 8u * buf, (gp >> 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sa = tmem + lane_base + 128u * buf + 64u * h;   // this warp's 64 columns
+                const int tok = ci.tok0 + 128 * j + 64 * h;
+                const int nvalid = min(64, ci.tok1 - tok);   // <= 0: this half of a short last pair
+                float alpha = 1.f;
+                bool need = false;
+                if (active) {
+                    uint32_t t[64];
+                    tmem_ld64(sa, t);
                     tmem_wait_ld();
-                } else {
+                    if (nvalid < 64 || tok + 64 > ci.L - p.q_len + 1) {
+                        const int lim = min(nvalid, vis - tok);   // in this warp's tokens
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = 0u;
-                }
-                if (!real) continue;
-                const int d0 = 64 * hw + 16 * qq;
-                float o[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    o[e] = n_sub > 0 ? (__uint_as_float(v[e]) + olo[col * kHeadDim + d0 + e]) * p.v_scale : 0.f;
-                if (p.direct) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float y = empty ? 0.f : o[e] / l_col;
-                        const int64_t oi = row * kHeadDim + d0 + e;
-                        if (p.out_dtype == 2)
-                            static_cast<float*>(p.out)[oi] = y;
-                        else if (p.out_dtype == 0)
-                            static_cast<__half*>(p.out)[oi] = __float2half_rn(y);
-                        else
-                            static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(y);
+                        for (int e = 0; e < 64; ++e)
+                            if (e >= lim) t[e] = __float_as_uint(-INFINITY);
                     }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.ws_u + (row * S + c.split) * kHeadDim + d0);
+                    float mx = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+                    for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(t[e]));
+                    // the pair's max over every warp holding the column, the same in
+                    // each (double-buffered by pair parity: every warp of the group has
+                    // read a slot before the group passes its next exchange)
+                    float* xm = xmax + buf * 256;
+                    xm[xslot] = mx;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_x);
+                    ok = __all_sync(kFull, wait_or_flag(b_x, gp & 1));
+                    if (!ok) break;
+                    if (kStack)
+                        mx = fmaxf(fmaxf(xm[col], xm[64 + col]), fmaxf(xm[128 + col], xm[192 + col]));
+                    else
+                        mx = fmaxf(xm[r], xm[128 + r]);
+                    mx *= sc;                      // raw scores: sc > 0 keeps the max
+                    need = mx > m_run + 8.f;       // also true for the first finite max
+                    if (need) {
+                        alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mx);
+                        l_run *= alpha;
+                        m_run = mx;
+                    }
+                    const float mu = m_run == -INFINITY ? 0.f : m_run;
+                    // P over the scores' columns, 32 tokens at a time: hi parts at
+                    // columns 0-31 of the warp's 64, lo parts at 32-63 (KIND 32: each
+                    // side keeps its own part at 0-31)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(t[32 * hf + 2 * e]), sc, -mu));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(t[32 * hf + 2 * e + 1]), sc, -mu));
+                            l_run += p0 + p1;
+                            float k0, k1, d0, d1;
+                            hi[e] = Mma<T>::pack(p0, p1, k0, k1);
+                            lo[e] = Mma<T>::pack(p0 - k0, p1 - k1, d0, d1);
+                        }
+                        if (kStack) {
+                            if (side == 0)
+                                tmem_st16(sa + 16u * hf, hi);
+                            else
+                                tmem_st16(sa + 16u * hf, lo);
+                        } else {
+                            tmem_st16(sa + 16u * hf, hi);
+                            tmem_st16(sa + 32u + 16u * hf, lo);
+                        }
+                    }
+                }
+                if (j > 0 && active && __any_sync(kFull, need)) {
+                    // O is rescaled once PV of the previous pair is done with it:
+                    // this lane's O row, dims 64 h .. 64 h + 63
+                    ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * (buf ^ 1), ((gp - 1) >> 1) & 1));
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int qq = 0; qq < 4; ++qq) {
+                            uint32_t v[16];
+                            const uint32_t ta = tmem_o + lane_base + 64u * h + 16u * qq;
+                            tmem_ld16(ta, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            tmem_st16(ta, v);
+                        }
+                    }
+                }
+                tmem_wait_st();
+                if (!ok) break;
+                // V rows past the end of a loaded stage hold whatever the cache holds
+                // there; P is 0 for them, but 0 * NaN would still poison PV
+                const int slot_base = (gp % kPairSlots) * 4 * static_cast<int>(kRegion);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (2 * j + hh >= ci.n_sub) break;
+                    const int nv = min(64, ci.tok1 - (ci.tok0 + 128 * j + 64 * hh));
+                    if (nv >= 64) continue;
+                    for (int idx = threadIdx.x; idx < (64 - nv) * 16; idx += kSoftmaxThreads) {
+                        const int row = 64 * hh + nv + (idx >> 4), ch = idx & 15;
+                        *reinterpret_cast<uint4*>(c.smem + slot_base + (2 + (ch >> 3)) * kRegion + row * 128 +
+                                                  (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_p_full + 8u * buf);
+                // the next non-empty item's Q goes to the other buffer, whose last
+                // reader (S of the item before this one) completed before this
+                // item's first scores
+                if (j == min(1, n_pairs - 1)) {
+                    wq.next();               // from this item's pairs ...
+                    while (!wq.done && wq.j != 0) wq.next();   // ... to the next item
+                    if (!wq.done) stage_q(wq.c, kq + 1);
                 }
             }
-            if (real && hw == 0) {
-                if (p.direct) {
-                    if (p.lse != nullptr) p.lse[row] = empty ? -INFINITY : m_out + logf(l_col);
-                } else {
-                    p.ws_m[row * S + c.split] = m_out;
-                    p.ws_l[row * S + c.split] = l_col;
+            // ---- the item's epilogue: once the last PV is done, O read out and
+            // the column states written; O is then handed back to PV
+            if (ok) {
+                ok = __all_sync(kFull, wait_or_flag(b_o_done + 8u * ((gp - 1) & 1), ((gp - 1) >> 1) & 1));
+                tc_fence_after();
+            }
+            if (!ok) *sm_abort = 1;
+            xsum[xslot] = l_run;
+            named_sync(1, kSoftmaxThreads);
+            if (*sm_abort != 0) break;   // every softmax warp leaves together
+            const float m_out = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
+            const float l_col = kStack ? xsum[col] + xsum[64 + col] : xsum[r] + xsum[128 + r];
+            const bool empty = m_out == -INFINITY || !(l_col > 0.f);
+            const int64_t my_row = real ? (static_cast<int64_t>(ci.b) * p.q_len + col / p.group) * p.n_q_heads +
+                                              ci.kvh * p.group + col % p.group
+                                        : 0;
+            if (kStack) {
+                // O's lo rows (at most 2^-9 of the result) pass to the hi side as
+                // bf16 pairs, [column][dim pair] with rows padded to 68 words, so
+                // that each 8-lane phase of a 16-byte access meets distinct banks
+                if (side == 1 && active) {
+                    uint32_t v[64];
+                    tmem_ld64(tmem_o + lane_base + 64u * h, v);
+                    tmem_wait_ld();
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const __nv_bfloat162 w = __floats2bfloat162_rn(__uint_as_float(v[2 * e]),
+                                                                       __uint_as_float(v[2 * e + 1]));
+                        memcpy(&pk[e], &w, 4);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(olo_w + col * kOloRow + 32 * h);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+                named_sync(1, kSoftmaxThreads);
+            }
+            // tcgen05.ld is warp-wide: every lane loads; lanes past the columns
+            // stage values nobody stores
+            if (side == 0 && active) {
+                float* sg = stg + (kStack ? (q & 1) * 2 + h : warp) * kStgWarp;   // [16 rows][36]
+                // four steps of 16 rows x 32 dims: the rows' lanes stage their values,
+                // then lane l stores dims 4 (l % 8) .. +3 of row l / 8 + 4 k, so a
+                // store covers four whole 128-byte lines.  The loop stays rolled: it
+                // runs once per item, and its code is fetched cold each time.
+#pragma unroll 1
+                for (int step = 0; step < 4; ++step) {
+                    const int rh = step >> 1, dh = step & 1;
+                    uint32_t v[32];
+                    tmem_ld32(tmem_o + lane_base + 64u * h + 32u * dh, v);
+                    tmem_wait_ld();
+                    if ((lane >> 4) == rh) {
+                        // this row's 32 values: the state's u (values are v_scale x the
+                        // stored ones), or out with one split
+                        float o[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]);
+                        if (kStack) {
+                            const uint4* lw = reinterpret_cast<const uint4*>(olo_w + col * kOloRow + 32 * h + 16 * dh);
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const uint4 w4 = lw[x];
+                                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    o[8 * x + 2 * t] += __uint_as_float(w[t] << 16);
+                                    o[8 * x + 2 * t + 1] += __uint_as_float(w[t] & 0xffff0000u);
+                                }
+                            }
+                        }
+                        // (a uniform branch: the division is only paid for with one split)
+                        if (!p.direct) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] *= p.v_scale;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : (o[e] * p.v_scale) / l_col;
+                        }
+                        float4* sr = reinterpret_cast<float4*>(sg + (lane & 15) * kStgRow);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) sr[x] = make_float4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+                    }
+                    __syncwarp();
+                    // every row and value is read before any store is issued (the
+                    // compiler cannot move shared loads above a global store)
+                    const int f = lane & 7, d0 = 64 * h + 32 * dh + 4 * f;
+                    int64_t rows[4];
+                    bool rreal[4];
+                    float y[4][4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = (lane >> 3) + 4 * k;     // row within the step's 16
+                        rows[k] = __shfl_sync(kFull, my_row, 16 * rh + rr);
+                        rreal[k] = __shfl_sync(kFull, real ? 1 : 0, 16 * rh + rr) != 0;
+                        const float4 y4 = *reinterpret_cast<const float4*>(sg + rr * kStgRow + 4 * f);
+                        y[k][0] = y4.x;
+                        y[k][1] = y4.y;
+                        y[k][2] = y4.z;
+                        y[k][3] = y4.w;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (!rreal[k]) continue;
+                        if (!p.direct) {
+                            *reinterpret_cast<float4*>(p.ws_u + (rows[k] * S + ci.split) * kHeadDim + d0) =
+                                make_float4(y[k][0], y[k][1], y[k][2], y[k][3]);
+                        } else {   // out carries only its element alignment: scalar stores
+                            const int64_t oi = rows[k] * kHeadDim + d0;
+                            if (p.out_dtype == 2) {
+                                float* o = static_cast<float*>(p.out) + oi;
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) o[t] = y[k][t];
+                            } else if (p.out_dtype == 0) {
+                                __half* o = static_cast<__half*>(p.out) + oi;
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) o[t] = __float2half_rn(y[k][t]);
+                            } else {
+                                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + oi;
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) o[t] = __float2bfloat16_rn(y[k][t]);
+                            }
+                        }
+                    }
+                    __syncwarp();   // the staging is rewritten by the next step
+                }
+                if (real && h == 0) {
+                    if (p.direct) {
+                        if (p.lse != nullptr) p.lse[my_row] = empty ? -INFINITY : m_out + logf(l_col);
+                    } else {
+                        p.ws_m[my_row * S + ci.split] = m_out;
+                        p.ws_l[my_row * S + ci.split] = l_col;
+                    }
                 }
             }
+            if (kStack) named_sync(1, kSoftmaxThreads);   // olo is rewritten by the next item
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_o_free);
+            ++kq;
+            named_sync(1, kSoftmaxThreads);   // every warp has read sm_abort before the next item
         }
+        if (!ok) *c.cons_abort = 1;
     }
     // every tensor-memory user is done (the MMA thread waited for its last commit)
     tc_fence_before();
@@ -1952,13 +1979,17 @@ static cudaError_t launch_split_dt(const CUtensorMap& tmK, const CUtensorMap& tm
 template <typename T, int KIND>
 static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
                                     int batch, int n_kv_heads, cudaStream_t stream) {
-    auto kern = KIND == 32 ? fd_split_umma64_kernel<T> : fd_split_umma_kernel<T>;
+    auto kern = fd_split_umma_kernel<T, KIND>;
     const size_t smem = Geo<KIND>::kSmem;
     static std::atomic<unsigned long long> configured_ctx{0};
     cudaError_t e = allow_smem(kern, smem, configured_ctx);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
-                      dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
+    // persistent: one CTA per SM (one per item if there are fewer items)
+    const int sms = fd_num_sms(-1);
+    if (sms < 1) return cudaErrorInvalidDevice;
+    const int64_t items = static_cast<int64_t>(p.n_splits) * n_kv_heads * batch;
+    const int ctas = static_cast<int>(items < sms ? items : sms);
+    return launch_pdl(kern, dim3(ctas), dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
 cudaError_t launch_split(const CUtensorMap& tmK, const CUtensorMap& tmV, const SplitParams& p,
