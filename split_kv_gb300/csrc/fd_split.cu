@@ -187,9 +187,8 @@ struct Geo {
     // tcgen05: KIND 32's exchange of O's lo rows (17 KB), then the softmax
     // exchange and the tcgen05 barriers (4 KB)
     static constexpr int kOloBytes = KIND == 32 ? 64 * 68 * 4 : 0;
-    // + the epilogue's per-warp staging of states ([16][36] floats; KIND 32
-    // writes with its four hi-side warps)
-    static constexpr int kStgBytes = KIND == 31 ? 8 * 16 * 36 * 4 : KIND == 32 ? 4 * 16 * 36 * 4 : 0;
+    // + KIND 31's per-warp staging of states in the epilogue ([16][36] floats)
+    static constexpr int kStgBytes = KIND == 31 ? 8 * 16 * 36 * 4 : 0;
     static constexpr int kExtraBytes = kUmma ? kOloBytes + kStgBytes + 4096 : 0;
     static constexpr int kOffBars = kOffExtra + kExtraBytes;   // full[kRing], empty[kRing]
     static constexpr bool kOwnMap = kF8 || kUmma;
@@ -1813,27 +1812,20 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
             // tcgen05.ld is warp-wide: every lane loads; lanes past the columns
             // stage values nobody stores
             if (side == 0 && active) {
-                float* sg = stg + (kStack ? (q & 1) * 2 + h : warp) * kStgWarp;   // [16 rows][36]
-                // four steps of 16 rows x 32 dims: the rows' lanes stage their values,
-                // then lane l stores dims 4 (l % 8) .. +3 of row l / 8 + 4 k, so a
-                // store covers four whole 128-byte lines.  The loop stays rolled: it
-                // runs once per item, and its code is fetched cold each time.
-#pragma unroll 1
-                for (int step = 0; step < 4; ++step) {
-                    const int rh = step >> 1, dh = step & 1;
-                    uint32_t v[32];
-                    tmem_ld32(tmem_o + lane_base + 64u * h + 32u * dh, v);
+                if constexpr (kStack) {
+                    // each lane writes its own row's 64 dims: 16 independent 16-byte
+                    // stores from registers (the row's 256 bytes are contiguous)
+                    uint32_t v[64];
+                    tmem_ld64(tmem_o + lane_base + 64u * h, v);
                     tmem_wait_ld();
-                    if ((lane >> 4) == rh) {
-                        // this row's 32 values: the state's u (values are v_scale x the
-                        // stored ones), or out with one split
-                        float o[32];
+                    if (real) {
+                        float o[64];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]);
+                        for (int e = 0; e < 64; ++e) o[e] = __uint_as_float(v[e]);
                         if (kStack) {
-                            const uint4* lw = reinterpret_cast<const uint4*>(olo_w + col * kOloRow + 32 * h + 16 * dh);
+                            const uint4* lw = reinterpret_cast<const uint4*>(olo_w + col * kOloRow + 32 * h);
 #pragma unroll
-                            for (int x = 0; x < 4; ++x) {
+                            for (int x = 0; x < 8; ++x) {
                                 const uint4 w4 = lw[x];
                                 const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
@@ -1843,60 +1835,100 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
                                 }
                             }
                         }
-                        // (a uniform branch: the division is only paid for with one split)
                         if (!p.direct) {
+                            float4* dst = reinterpret_cast<float4*>(p.ws_u + (my_row * S + ci.split) * kHeadDim + 64 * h);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= p.v_scale;
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : (o[e] * p.v_scale) / l_col;
-                        }
-                        float4* sr = reinterpret_cast<float4*>(sg + (lane & 15) * kStgRow);
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) sr[x] = make_float4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
-                    }
-                    __syncwarp();
-                    // every row and value is read before any store is issued (the
-                    // compiler cannot move shared loads above a global store)
-                    const int f = lane & 7, d0 = 64 * h + 32 * dh + 4 * f;
-                    int64_t rows[4];
-                    bool rreal[4];
-                    float y[4][4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int rr = (lane >> 3) + 4 * k;     // row within the step's 16
-                        rows[k] = __shfl_sync(kFull, my_row, 16 * rh + rr);
-                        rreal[k] = __shfl_sync(kFull, real ? 1 : 0, 16 * rh + rr) != 0;
-                        const float4 y4 = *reinterpret_cast<const float4*>(sg + rr * kStgRow + 4 * f);
-                        y[k][0] = y4.x;
-                        y[k][1] = y4.y;
-                        y[k][2] = y4.z;
-                        y[k][3] = y4.w;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (!rreal[k]) continue;
-                        if (!p.direct) {
-                            *reinterpret_cast<float4*>(p.ws_u + (rows[k] * S + ci.split) * kHeadDim + d0) =
-                                make_float4(y[k][0], y[k][1], y[k][2], y[k][3]);
+                            for (int x = 0; x < 16; ++x)
+                                dst[x] = make_float4(o[4 * x] * p.v_scale, o[4 * x + 1] * p.v_scale,
+                                                     o[4 * x + 2] * p.v_scale, o[4 * x + 3] * p.v_scale);
                         } else {   // out carries only its element alignment: scalar stores
-                            const int64_t oi = rows[k] * kHeadDim + d0;
-                            if (p.out_dtype == 2) {
-                                float* o = static_cast<float*>(p.out) + oi;
+                            const int64_t oi = my_row * kHeadDim + 64 * h;
 #pragma unroll
-                                for (int t = 0; t < 4; ++t) o[t] = y[k][t];
-                            } else if (p.out_dtype == 0) {
-                                __half* o = static_cast<__half*>(p.out) + oi;
-#pragma unroll
-                                for (int t = 0; t < 4; ++t) o[t] = __float2half_rn(y[k][t]);
-                            } else {
-                                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + oi;
-#pragma unroll
-                                for (int t = 0; t < 4; ++t) o[t] = __float2bfloat16_rn(y[k][t]);
+                            for (int e = 0; e < 64; ++e) {
+                                const float y = empty ? 0.f : (o[e] * p.v_scale) / l_col;
+                                if (p.out_dtype == 2)
+                                    static_cast<float*>(p.out)[oi + e] = y;
+                                else if (p.out_dtype == 0)
+                                    static_cast<__half*>(p.out)[oi + e] = __float2half_rn(y);
+                                else
+                                    static_cast<__nv_bfloat16*>(p.out)[oi + e] = __float2bfloat16_rn(y);
                             }
                         }
                     }
-                    __syncwarp();   // the staging is rewritten by the next step
+                } else {
+                    // 65-128 columns: all eight warps write, so whole 128-byte lines pay off
+                    float* sg = stg + warp * kStgWarp;   // [16 rows][36]
+                    // four steps of 16 rows x 32 dims: the rows' lanes stage their values,
+                    // then lane l stores dims 4 (l % 8) .. +3 of row l / 8 + 4 k, so a
+                    // store covers four whole 128-byte lines.  The loop stays rolled: it
+                    // runs once per item, and its code is fetched cold each time.
+#pragma unroll 1
+                    for (int step = 0; step < 4; ++step) {
+                        const int rh = step >> 1, dh = step & 1;
+                        uint32_t v[32];
+                        tmem_ld32(tmem_o + lane_base + 64u * h + 32u * dh, v);
+                        tmem_wait_ld();
+                        if ((lane >> 4) == rh) {
+                            // this row's 32 values: the state's u (values are v_scale x the
+                            // stored ones), or out with one split
+                            float o[32];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]);
+                            // (a uniform branch: the division is only paid for with one split)
+                            if (!p.direct) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] *= p.v_scale;
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] = empty ? 0.f : (o[e] * p.v_scale) / l_col;
+                            }
+                            float4* sr = reinterpret_cast<float4*>(sg + (lane & 15) * kStgRow);
+#pragma unroll
+                            for (int x = 0; x < 8; ++x) sr[x] = make_float4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+                        }
+                        __syncwarp();
+                        // every row and value is read before any store is issued (the
+                        // compiler cannot move shared loads above a global store)
+                        const int f = lane & 7, d0 = 64 * h + 32 * dh + 4 * f;
+                        int64_t rows[4];
+                        bool rreal[4];
+                        float y[4][4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int rr = (lane >> 3) + 4 * k;     // row within the step's 16
+                            rows[k] = __shfl_sync(kFull, my_row, 16 * rh + rr);
+                            rreal[k] = __shfl_sync(kFull, real ? 1 : 0, 16 * rh + rr) != 0;
+                            const float4 y4 = *reinterpret_cast<const float4*>(sg + rr * kStgRow + 4 * f);
+                            y[k][0] = y4.x;
+                            y[k][1] = y4.y;
+                            y[k][2] = y4.z;
+                            y[k][3] = y4.w;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (!rreal[k]) continue;
+                            if (!p.direct) {
+                                *reinterpret_cast<float4*>(p.ws_u + (rows[k] * S + ci.split) * kHeadDim + d0) =
+                                    make_float4(y[k][0], y[k][1], y[k][2], y[k][3]);
+                            } else {   // out carries only its element alignment: scalar stores
+                                const int64_t oi = rows[k] * kHeadDim + d0;
+                                if (p.out_dtype == 2) {
+                                    float* o = static_cast<float*>(p.out) + oi;
+#pragma unroll
+                                    for (int t = 0; t < 4; ++t) o[t] = y[k][t];
+                                } else if (p.out_dtype == 0) {
+                                    __half* o = static_cast<__half*>(p.out) + oi;
+#pragma unroll
+                                    for (int t = 0; t < 4; ++t) o[t] = __float2half_rn(y[k][t]);
+                                } else {
+                                    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + oi;
+#pragma unroll
+                                    for (int t = 0; t < 4; ++t) o[t] = __float2bfloat16_rn(y[k][t]);
+                                }
+                            }
+                        }
+                        __syncwarp();   // the staging is rewritten by the next step
+                    }
                 }
                 if (real && h == 0) {
                     if (p.direct) {
