@@ -126,8 +126,11 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
 // Many rows (query blocks): one warp per row, four rows per CTA, so thousands
 // of rows fit in one wave instead of queueing CTAs of four warps.  Lane l
 // holds dims 4l .. 4l + 3 and the m, l of splits l, l + 32, ...; the partial
-// outputs are requested kPre splits at a time and added in split order.
+// outputs of the first kPreRows splits are requested together with m and l
+// (one round trip to memory up to 16 splits), the rest kPre at a time, and
+// they are added in split order.
 constexpr int kRowsPerCta = 4;
+constexpr int kPreRows = 16;
 
 __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const CombineParams p) {
     grid_dependency_trigger();
@@ -139,9 +142,9 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const
     const int64_t base = static_cast<int64_t>(row) * S;
     const float4* urow = reinterpret_cast<const float4*>(p.ws_u + base * kHeadDim) + lane;
     constexpr int kStride = kHeadDim / 4;   // float4s per split
-    float4 pre[kPre];
+    float4 pre[kPreRows];
 #pragma unroll
-    for (int k = 0; k < kPre; ++k) pre[k] = k < S ? urow[k * kStride] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kPreRows; ++k) pre[k] = k < S ? urow[k * kStride] : make_float4(0.f, 0.f, 0.f, 0.f);
     float mv[kMaxSplits / 32], lv[kMaxSplits / 32];
 #pragma unroll
     for (int j = 0; j < kMaxSplits / 32; ++j) {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const
     };
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kPre; ++k) {
+    for (int k = 0; k < kPreRows; ++k) {
         const float wt = weight(k);
         if (k < S) {
             a.x = fmaf(wt, pre[k].x, a.x);
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const
             a.w = fmaf(wt, pre[k].w, a.w);
         }
     }
-    for (int i0 = kPre; i0 < S; i0 += kPre) {
+    for (int i0 = kPreRows; i0 < S; i0 += kPre) {
         float4 u[kPre];
 #pragma unroll
         for (int k = 0; k < kPre; ++k)
