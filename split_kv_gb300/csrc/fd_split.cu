@@ -1073,6 +1073,17 @@ template <typename T> struct Consumer<T, 18> {
     static __device__ bool run(const SplitCtx& c, int w, int l) { return consume_simt<T, 8>(c, w, l); }
 };
 
+// Split `split` of S over L tokens: the tokens [tok0, tok1) of its share of
+// the ceil(L / unit) units, the first L mod S shares one unit longer.
+__device__ __forceinline__ void split_tokens(int L, int S, int unit, int split, int& tok0, int& tok1) {
+    const int n_units = (L + unit - 1) / unit;
+    const int base = n_units / S, rem = n_units % S;
+    const int u_begin = split * base + (split < rem ? split : rem);
+    const int u_count = base + (split < rem ? 1 : 0);
+    tok0 = u_begin * unit;
+    tok1 = min((u_begin + u_count) * unit, L);
+}
+
 // The token range of split `split` of sequence b (KV head kvh): the sequence
 // cut into S balanced ranges of whole 16-token units (8 for 8-token pages), so
 // no TMA box straddles a page and a paged cache splits exactly like a
@@ -1089,22 +1100,49 @@ __device__ __forceinline__ void split_range(SplitCtx& c, int b, int kvh, int spl
         L = L < 0 ? 0 : p.capacity;
     }
     c.L = L;
-    const int S = p.n_splits;
-    const int unit = p.split_unit;
-    const int n_units = (L + unit - 1) / unit;
-    const int base = n_units / S, rem = n_units % S;
-    const int u_begin = split * base + (split < rem ? split : rem);
-    const int u_count = base + (split < rem ? 1 : 0);
-    c.tok0 = u_begin * unit;
-    c.tok1 = min((u_begin + u_count) * unit, L);
+    split_tokens(L, p.n_splits, p.split_unit, split, c.tok0, c.tok1);
     c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Geo<KIND>::kSub - 1) / Geo<KIND>::kSub : 0;
+}
+
+// Tokens the L2 prefetch ahead of the launch wait covers per CTA.
+constexpr int kPrefetchTokens = 256;
+
+// Ahead of the launch wait: the first tokens of one split into L2, so that
+// its first stages are served from L2 once the wait ends.  The length comes
+// from a relaxed load, since the kernel before this one may still be writing
+// it; a stale length only misplaces the prefetch, never a result (every load
+// after the wait reads the length again).  Contiguous caches only: a block
+// table is read only after the wait.
+template <int KIND>
+__device__ __forceinline__ void prefetch_split(const SplitParams& p, const CUtensorMap* tmK,
+                                               const CUtensorMap* tmV, int b, int kvh, int split) {
+    using Gm = Geo<KIND>;
+    if (p.page_size != 0) return;
+    int L = ld_relaxed_s32(p.seqlens + b);
+    L = L < 0 ? 0 : (L > p.capacity ? p.capacity : L);
+    int t0, t1;
+    split_tokens(L, p.n_splits, p.split_unit, split, t0, t1);
+    t1 = min(t1, t0 + kPrefetchTokens);
+#pragma unroll 1
+    for (int t = t0; t < t1; t += Gm::kSub) {
+        if (Gm::kF8) {
+            tma_prefetch_4d(tmK, 0, t, kvh, b);
+            tma_prefetch_4d(tmV, 0, t, kvh, b);
+        } else {
+            tma_prefetch_4d(tmK, 0, t, kvh, b);
+            tma_prefetch_4d(tmK, 64, t, kvh, b);
+            tma_prefetch_4d(tmV, 0, t, kvh, b);
+            tma_prefetch_4d(tmV, 64, t, kvh, b);
+        }
+    }
 }
 
 // The start every split kernel shares: the context, the ring's barriers and
 // the programmatic-dependent-launch wait.
 template <int KIND>
 __device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const SplitParams& p,
-                                            const CUtensorMap* tmK, const CUtensorMap* tmV) {
+                                            const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                            int pf_b, int pf_kvh, int pf_split) {
     using Gm = Geo<KIND>;
     constexpr int kRing = Gm::kRing;
     c.stages = kRing;
@@ -1130,6 +1168,8 @@ __device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const Sp
     if (warp == Gm::kWarps && lane == 0) {
         prefetch_tensormap(tmK);
         prefetch_tensormap(tmV);
+        // (pf_b < 0: a column block after the first, whose sibling prefetches)
+        if (pf_b >= 0) prefetch_split<KIND>(p, tmK, tmV, pf_b, pf_kvh, pf_split);
     }
     // Programmatic dependent launch: let the combine kernel that follows get
     // resident now, and wait for whatever preceded this kernel in the stream
@@ -1144,7 +1184,8 @@ __device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const Sp
 template <int KIND>
 __device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const SplitParams& p,
                                             const CUtensorMap* tmK, const CUtensorMap* tmV) {
-    split_setup<KIND>(c, smem, p, tmK, tmV);
+    split_setup<KIND>(c, smem, p, tmK, tmV, blockIdx.x % p.col_blocks == 0 ? static_cast<int>(blockIdx.z) : -1,
+                      blockIdx.y, blockIdx.x / p.col_blocks);
     split_range<KIND>(c, blockIdx.z, blockIdx.y, blockIdx.x / p.col_blocks,
                       threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0);
     c.cb = blockIdx.x % p.col_blocks;
@@ -1417,11 +1458,12 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     SplitCtx c;
-    split_setup<KIND>(c, smem, p, &tmK, &tmV);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const int S = p.n_splits;
     const int n_items = S * p.n_kv_heads * p.batch;
+    // (no L2 prefetch ahead of the launch wait: measured slower here)
+    split_setup<KIND>(c, smem, p, &tmK, &tmV, -1, 0, 0);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     // KIND 32: O's lo rows pass through shared memory, [64 columns][68 words] of bf16 pairs
     uint32_t* olo_w = reinterpret_cast<uint32_t*>(smem + Gm::kOffExtra);
     // the epilogue's staging of a warp's 16 rows x 32 dims, rows padded to 36
