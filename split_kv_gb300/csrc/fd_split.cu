@@ -1104,7 +1104,8 @@ __device__ __forceinline__ void split_range(SplitCtx& c, int b, int kvh, int spl
     c.n_sub = c.tok1 > c.tok0 ? (c.tok1 - c.tok0 + Geo<KIND>::kSub - 1) / Geo<KIND>::kSub : 0;
 }
 
-// Tokens the L2 prefetch ahead of the launch wait covers per CTA.
+// Tokens the L2 prefetch ahead of the launch wait covers per CTA: half the
+// split, at most this many (measured: more delays the first stages).
 constexpr int kPrefetchTokens = 256;
 
 // Ahead of the launch wait: the first tokens of one split into L2, so that
@@ -1122,7 +1123,7 @@ __device__ __forceinline__ void prefetch_split(const SplitParams& p, const CUten
     L = L < 0 ? 0 : (L > p.capacity ? p.capacity : L);
     int t0, t1;
     split_tokens(L, p.n_splits, p.split_unit, split, t0, t1);
-    t1 = min(t1, t0 + kPrefetchTokens);
+    t1 = min(t1, t0 + min(kPrefetchTokens, max(Gm::kSub, (t1 - t0) / 2)));
 #pragma unroll 1
     for (int t = t0; t < t1; t += Gm::kSub) {
         if (Gm::kF8) {
