@@ -1578,6 +1578,10 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {   // 16 tokens per MMA
                     if (kk == 4 && !two) break;
+                    // 17-64 columns: the pair's first stage is read by the MMAs so far, so
+                    // its slot refills while the second stage's MMAs run (with 65-128
+                    // columns the earlier refill measured slower)
+                    if (kStack && kk == 4) umma_commit(c.empty_bar((2 * gpv) % kRing));
                     // tokens 16 kk .. +15 were written by the warps of token half kk / 4:
                     // hi at columns 64 (kk / 4) + 8 (kk % 4), lo 32 columns further
                     const uint32_t a = pa + 64u * (kk >> 2) + 8u * (kk & 3);
@@ -1586,8 +1590,8 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
                     if (!kStack) umma_f16_ta(tmem_o, a + 32u, b, id_o, true);
                 }
                 umma_commit(b_o_done + 8u * static_cast<uint32_t>(gpv & 1));
-                umma_commit(c.empty_bar((2 * gpv) % kRing));        // both slots, filled or not
-                umma_commit(c.empty_bar((2 * gpv + 1) % kRing));
+                if (!kStack || !two) umma_commit(c.empty_bar((2 * gpv) % kRing));
+                umma_commit(c.empty_bar((2 * gpv + 1) % kRing));    // filled or not
                 wv.next();
                 ++gpv;
                 if (boundary) {
@@ -2059,11 +2063,16 @@ static cudaError_t launch_split_umma(const CUtensorMap& tmK, const CUtensorMap& 
     static std::atomic<unsigned long long> configured_ctx{0};
     cudaError_t e = allow_smem(kern, smem, configured_ctx);
     if (e != cudaSuccess) return e;
-    // persistent: one CTA per SM (one per item if there are fewer items)
+    // persistent: at most one CTA per SM, and as many CTAs as give every CTA
+    // the same number of items (one more for some at most): 288 items on 152
+    // SMs run as 144 CTAs of two, rather than 136 of two beside 16 of one
+    // that idle through the second half while an SM's own streaming rate
+    // holds the other 136 below the memory's
     const int sms = fd_num_sms(-1);
     if (sms < 1) return cudaErrorInvalidDevice;
     const int64_t items = static_cast<int64_t>(p.n_splits) * n_kv_heads * batch;
-    const int ctas = static_cast<int>(items < sms ? items : sms);
+    const int64_t per_cta = (items + sms - 1) / sms;
+    const int ctas = static_cast<int>((items + per_cta - 1) / per_cta);
     return launch_pdl(kern, dim3(ctas), dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
 }
 
