@@ -45,8 +45,8 @@
  *    one column of the CTA's tensor-core tile.  Up to 16 columns: one CTA per
  *    split on warp MMAs.  17-128 columns with a 16-bit cache (and no
  *    FD_FLAG_CUDA_CORES): one CTA per split on tcgen05 MMAs, all columns as
- *    the M rows of one 128-row tile (launched as a persistent grid of one CTA
- *    per SM that serves the splits in turn).  Otherwise ceil(G*q_len/16) CTAs per
+ *    the M rows of one 128-row tile (launched as a persistent grid of at most
+ *    one CTA per SM that serves the splits in turn).  Otherwise ceil(G*q_len/16) CTAs per
  *    split, each reading the split's K/V once.
  *  - Supported shapes: head_dim 128; G = n_q_heads / n_kv_heads and q_len
  *    with G*q_len <= 256 and q_len <= 16 (with FD_FLAG_CUDA_CORES: G in

@@ -1422,7 +1422,8 @@ struct PairWalk {
 //     hold column c's scores again; lanes 0-63 of P hold the hi parts and
 //     lanes 64-127 the lo parts, so one MMA per 16 tokens accumulates both
 //     (8 per pair), and O[c] + O[64 + c] is the result.
-// Persistent: the grid is one CTA per SM (or per work item if fewer), and CTA
+// Persistent: the grid is at most one CTA per SM, as many as give every CTA
+// the same number of work items (one fewer for some), and CTA
 // c serves the work items (split, KV head, sequence) c, c + gridDim.x, ...
 // back to back -- the producer streams the next item's stages without a
 // break, the next item's Q goes to the second Q buffer while the current item
