@@ -545,13 +545,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Margin of the lazy running max (log2 units): weights stay below 2^8.
+constexpr float kLazyMax = 8.f;
+
 // Online softmax (base 2) of TILES 16-token tiles for up to 8 * NB columns,
 // and P^T of each tile as hi + lo B fragments of the PV MMAs.  s[t] holds tile
 // t's S^T (C fragments); csc[j][e] is the base-2 score scale of the lane's
 // column 8j + 2tig + e, which sees the keys before vis[j][e]; tile t starts at
 // key tok[t] and has nvalid[t] rows.  Without `masked` every row is taken as
 // visible to every column (a full tile and one query per sequence).  The
-// running max moves once per call.
+// running max moves at most once per call.
 // Returns whether any running max moved (the accumulators then take al).
 template <typename MT, int NB, int TILES>
 __device__ __forceinline__ bool softmax_tiles(const float (&s)[TILES][NB][4], const float (&csc)[NB][2],
@@ -582,16 +585,29 @@ __device__ __forceinline__ bool softmax_tiles(const float (&s)[TILES][NB][4], co
                 }
         }
         float pr[TILES][4];
+        // Lazy running max: it moves only when some score exceeds it by more
+        // than kLazyMax (log2 units), so p stays below 2^kLazyMax; until then the
+        // tile needs no max reduction across the lanes, only one vote.  Any
+        // reference point gives the same state (u, m, l) up to rounding.
+        float lmx[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            float mx = -INFINITY;
+            lmx[e] = -INFINITY;
 #pragma unroll
-            for (int x = 0; x < TILES; ++x) mx = fmaxf(mx, fmaxf(t[x][e], t[x][e + 2]));
+            for (int x = 0; x < TILES; ++x) lmx[e] = fmaxf(lmx[e], fmaxf(t[x][e], t[x][e + 2]));
+        }
+        const bool move = __any_sync(kFull, lmx[0] > m[j][0] + kLazyMax || lmx[1] > m[j][1] + kLazyMax);
 #pragma unroll
-            for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-            const float mn = fmaxf(m[j][e], mx);
+        for (int e = 0; e < 2; ++e) {
+            float mn = m[j][e];
+            if (move) {   // warp-uniform
+                float mx = lmx[e];
+#pragma unroll
+                for (int o = 4; o <= 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+                mn = fmaxf(mn, mx);
+            }
             const float mu = mn == -INFINITY ? 0.f : mn;   // never -inf - -inf
-            al[j][e] = fast_exp2(m[j][e] - mu);
+            al[j][e] = move ? fast_exp2(m[j][e] - mu) : 1.f;
             float sum = 0.f;
 #pragma unroll
             for (int x = 0; x < TILES; ++x) {
