@@ -195,6 +195,8 @@ struct Geo {
     static_assert(!kUmma || kSub == fdk::kSub, "the tcgen05 variant streams the 16-bit stages");
     static constexpr int kOffFlag = (kOwnMap ? kOffBars + 128 : fdk::kOffFlag);
     static constexpr int kSmem = (kOwnMap ? kOffFlag + 16 : kSmemUsed) + 1024;   // + alignment slack
+    // a CTA that serves two splits at once (see fd_split_kernel) gives each this much
+    static constexpr int kSmemHalf = (kSmem - 1024 + 1023) / 1024 * 1024;
     // + one TMA producer warp (+ one MMA-issuing warp for tcgen05)
     static constexpr int kThreads = (kWarps + (kUmma ? 2 : 1)) * 32;
     static constexpr int kEmptyArrivals = kUmma ? 1 : kWarps;  // tcgen05: the MMA commit
@@ -219,6 +221,7 @@ struct SplitCtx {
     int cb;                     // block of 16 (query, head) columns this CTA serves
     int L;                      // the sequence's length (keys in the cache)
     int tok0, tok1, n_sub;
+    int bar_id;                 // the consumer warps' named barrier (1, or 2 for a CTA's second half)
 
     __device__ __forceinline__ uint32_t full_bar(int s) const { return bar0 + 8u * s; }
     __device__ __forceinline__ uint32_t empty_bar(int s) const { return bar0 + 8u * (stages + s); }
@@ -446,7 +449,7 @@ __device__ __forceinline__ bool consume_simt(const SplitCtx& c, int cw, int lane
 
     // Only consumers write cons_abort, and only before this barrier, so every
     // consumer warp takes the same branch below.
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(c.bar_id, kConsumerWarps * 32);
     if (*c.cons_abort) return false;   // states are not written after a timeout
     float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
     float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
@@ -801,7 +804,7 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) l[j][e] += __shfl_xor_sync(kFull, l[j][e], o);
 
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(c.bar_id, kConsumerWarps * 32);
     if (*c.cons_abort) return false;   // states are not written after a timeout
     float* wacc = reinterpret_cast<float*>(c.smem + kOffWAcc);
     float* wm = reinterpret_cast<float*>(c.smem + kOffWM);
@@ -1033,7 +1036,7 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) l[j][e] += __shfl_xor_sync(kFull, l[j][e], o);
 
-    named_sync(1, Gm::kWarps * 32);
+    named_sync(c.bar_id, Gm::kWarps * 32);
     if (*c.cons_abort) return false;   // states are not written after a timeout
     float* wacc = reinterpret_cast<float*>(c.smem);
     float* wm = reinterpret_cast<float*>(c.smem + Gm::kOffWM);
@@ -1159,19 +1162,21 @@ __device__ __forceinline__ void prefetch_split(const SplitParams& p, const CUten
 template <int KIND>
 __device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const SplitParams& p,
                                             const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                            int pf_b, int pf_kvh, int pf_split) {
+                                            int pf_b, int pf_kvh, int pf_split, int tid = threadIdx.x,
+                                            int half = 0) {
     using Gm = Geo<KIND>;
     constexpr int kRing = Gm::kRing;
     c.stages = kRing;
     c.p = &p;
     c.smem = smem;
     c.cb = 0;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    c.bar_id = 1 + half;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     c.bar0 = smem_u32(smem + Gm::kOffBars);
     c.abort_flag = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag);
     c.cons_abort = reinterpret_cast<volatile int*>(smem + Gm::kOffFlag + 4);
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < kRing; ++s) {
             mbar_init(c.full_bar(s), 1);
@@ -1195,34 +1200,46 @@ __device__ __forceinline__ void split_setup(SplitCtx& c, uint8_t* smem, const Sp
     grid_dependency_wait();
 }
 
-// split_setup and the token range of the CTA's split: grid (n_splits *
-// col_blocks, n_kv_heads, batch), the column blocks of one split adjacent, so
-// they run together and the later readers of the split's K/V find it in L2.
+// split_setup and the token range of the split of virtual block vx (x index
+// of the grid (n_splits * col_blocks, n_kv_heads, batch); vx < 0: none), the
+// column blocks of one split adjacent, so they run together and the later
+// readers of the split's K/V find it in L2.
 template <int KIND>
 __device__ __forceinline__ void split_begin(SplitCtx& c, uint8_t* smem, const SplitParams& p,
-                                            const CUtensorMap* tmK, const CUtensorMap* tmV) {
-    split_setup<KIND>(c, smem, p, tmK, tmV, blockIdx.x % p.col_blocks == 0 ? static_cast<int>(blockIdx.z) : -1,
-                      blockIdx.y, blockIdx.x / p.col_blocks);
-    split_range<KIND>(c, blockIdx.z, blockIdx.y, blockIdx.x / p.col_blocks,
-                      threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0);
-    c.cb = blockIdx.x % p.col_blocks;
+                                            const CUtensorMap* tmK, const CUtensorMap* tmV, int tid,
+                                            int half, int vx) {
+    split_setup<KIND>(c, smem, p, tmK, tmV, vx >= 0 && vx % p.col_blocks == 0 ? static_cast<int>(blockIdx.z) : -1,
+                      blockIdx.y, vx / p.col_blocks, tid, half);
+    if (vx < 0) return;
+    split_range<KIND>(c, blockIdx.z, blockIdx.y, vx / p.col_blocks, tid == 0 && vx == 0 && blockIdx.y == 0);
+    c.cb = vx % p.col_blocks;
 }
 
-template <typename T, int KIND>
-__global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
+// HALVES = 2: the CTA serves two splits at once, each with its own half of
+// the threads, shared memory, barriers and named barrier, so that every SM
+// holding work holds two splits (splits are otherwise placed one per SM
+// first, and where the consumers cannot keep up with HBM alone, the SMs left
+// with one split finish early while those with two set the kernel's time).
+template <typename T, int KIND, int HALVES>
+__global__ void __launch_bounds__(Geo<KIND>::kThreads * HALVES, HALVES == 1 ? 2 : 1)
     fd_split_kernel(const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
     using Gm = Geo<KIND>;
     constexpr int kWarps = Gm::kWarps;
     extern __shared__ uint8_t smem_raw[];
+    const int half = HALVES == 1 ? 0 : static_cast<int>(threadIdx.x) / Gm::kThreads;
+    const int tid = static_cast<int>(threadIdx.x) - half * Gm::kThreads;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023)) + half * Gm::kSmemHalf;
+    const int vx = static_cast<int>(blockIdx.x) * HALVES + half;
+    const bool idle = vx >= p.n_splits * p.col_blocks;   // the second half of the last CTA
     SplitCtx c;
-    split_begin<KIND>(c, smem, p, &tmK, &tmV);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    split_begin<KIND>(c, smem, p, &tmK, &tmV, tid, half, idle ? -1 : vx);
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int S = p.n_splits;
     __syncthreads();
+    if (idle) return;
 
     if (warp == kWarps) {
         produce<KIND>(c, &tmK, &tmV, lane);
@@ -1230,14 +1247,14 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 2)
     }
 
     if (!Consumer<T, KIND>::run(c, warp, lane)) return;
-    named_sync(1, kWarps * 32);
-    if (threadIdx.x >= kHeadDim) return;   // one thread per dim below
+    named_sync(c.bar_id, kWarps * 32);
+    if (tid >= kHeadDim) return;   // one thread per dim below
 
     // ---- merge the consumer warps' states of each column and write the split's state
     const float* wacc = reinterpret_cast<const float*>(smem);
     const float* wm = reinterpret_cast<const float*>(smem + Gm::kOffWM);
     const float* wl = reinterpret_cast<const float*>(smem + Gm::kOffWL);
-    const int d = threadIdx.x;   // 0 .. 127
+    const int d = tid;   // 0 .. 127
     const int ncols = min(kCols, p.cols - c.cb * kCols);
     for (int col = 0; col < ncols; ++col) {
         float M = -INFINITY;
@@ -2038,13 +2055,27 @@ template <typename T, int KIND>
 static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   const SplitParams& p, int batch, int n_kv_heads,
                                   cudaStream_t stream) {
-    auto kern = fd_split_kernel<T, KIND>;
-    const size_t smem = Geo<KIND>::kSmem;
+    using Gm = Geo<KIND>;
+    const int blocks = p.n_splits * p.col_blocks;
+    // fp8, up to 8 columns: its consumers do not keep up with HBM on an SM of
+    // their own, so once splits outnumber SMs every CTA takes two
+    if constexpr (KIND == 21) {
+        if (static_cast<int64_t>(blocks) * n_kv_heads * batch > fd_num_sms(-1)) {
+            auto kern = fd_split_kernel<T, KIND, 2>;
+            const size_t smem = 2 * Gm::kSmemHalf + 1024;
+            static std::atomic<unsigned long long> configured_ctx2{0};
+            cudaError_t e = allow_smem(kern, smem, configured_ctx2);
+            if (e != cudaSuccess) return e;
+            return launch_pdl(kern, dim3((blocks + 1) / 2, n_kv_heads, batch), dim3(2 * Gm::kThreads), smem,
+                              stream, tmK, tmV, p);
+        }
+    }
+    auto kern = fd_split_kernel<T, KIND, 1>;
+    const size_t smem = Gm::kSmem;
     static std::atomic<unsigned long long> configured_ctx{0};
     cudaError_t e = allow_smem(kern, smem, configured_ctx);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(p.n_splits * p.col_blocks, n_kv_heads, batch),
-                      dim3(Geo<KIND>::kThreads), smem, stream, tmK, tmV, p);
+    return launch_pdl(kern, dim3(blocks, n_kv_heads, batch), dim3(Gm::kThreads), smem, stream, tmK, tmV, p);
 }
 
 template <typename T, int KIND>

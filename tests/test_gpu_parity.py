@@ -499,24 +499,28 @@ def test_lse_chaining_two_halves_merged_externally():
     np.testing.assert_allclose(got_l, l_full, rtol=0, atol=2e-5)
 
 
-@pytest.mark.parametrize("kind", ["f16", "e4m3", "f16_g8_q4", "bf16_g16_q8"])
+@pytest.mark.parametrize("kind", ["f16", "e4m3", "e4m3_two_per_cta", "f16_g8_q4", "bf16_g16_q8"])
 def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     """The test hook drops the first K/V stage: the kernel's bounded wait runs
     out, the status word reports FD_ERR_DEVICE_TIMEOUT, nothing faults, and
     the next call on the same context is correct.  The 16-bit consumer, the
-    fp8 one (which waits for two stages per iteration), and both tcgen05
+    fp8 one (which waits for two stages per iteration; with 20 splits x 8
+    heads, more CTAs than SMs, each CTA serves two splits), and both tcgen05
     kernels (32 and 128 columns), whose MMA thread gives up on the missing
     stage and frees its tensor memory."""
     import time
-    if kind == "e4m3" and not hasattr(torch, "float8_e4m3fn"):
+    if kind.startswith("e4m3") and not hasattr(torch, "float8_e4m3fn"):
         pytest.skip("torch without float8_e4m3fn")
     G, ql = {"f16_g8_q4": (8, 4), "bf16_g16_q8": (16, 8)}.get(kind, (1, 1))
     dt = "bf16" if kind.startswith("bf16") else "f16"
-    B, Hkv, D, T = 1, 8 if G == 1 else 2, 128, 300
+    S = 20 if kind == "e4m3_two_per_cta" else 1
+    B, Hkv, D, T = 1, 8 if G == 1 else 2, 128, 300 * S
+    if S > 1:
+        assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
     Hq = Hkv * G
     q = fd_inputs.randn((B, ql, Hq, D) if ql > 1 else (B, Hq, D), dt, 1201, device=DEV)
     sc = {}
-    if kind == "e4m3":
+    if kind.startswith("e4m3"):
         k = fd_inputs.randn_fp8((B, Hkv, T, D), 1203, device=DEV, gain=16.0)
         v = fd_inputs.randn_fp8((B, Hkv, T, D), 1204, device=DEV, gain=16.0)
         sc = dict(k_scale=1 / 16, v_scale=1 / 16)
@@ -524,9 +528,9 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
         k, v = _cache(B, Hkv, T, D, dt, 1202)
     sl_h = np.array([T], dtype=np.int32)
     seqlens = torch.from_numpy(sl_h).to(DEV)
-    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=1, **sc)
+    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=S, **sc)
     desc.flags = fd.FD_FLAG_TEST_DROP_FIRST_STAGE
-    ws = torch.empty(fd.fd_workspace_size(desc, 1), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(fd.fd_workspace_size(desc, S), dtype=torch.uint8, device=DEV)
     out = torch.zeros(B, ql, Hq, D, dtype=torch.float32, device=DEV)
     assert fd.fd_device_status(clear=True) == fd.FD_OK
     t0 = time.time()
@@ -535,7 +539,7 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     assert time.time() - t0 < 60
     assert fd.fd_device_status(clear=True) == fd.FD_OK
     got_o, got_l, _ = run_decode(q, k, v, sl_h, n_splits=1, **sc)
-    ref_o, ref_l = oracle_all(q, k, v, sl_h, dt, Hkv, kv_dtype=kind if kind == "e4m3" else None,
+    ref_o, ref_l = oracle_all(q, k, v, sl_h, dt, Hkv, kv_dtype="e4m3" if kind.startswith("e4m3") else None,
                               **sc)
     assert_parity(got_o, got_l, ref_o, ref_l, f"after a timed-out call ({kind})")
 
@@ -732,6 +736,28 @@ def test_fp8_cache(q_dtype, group):
     for S in (0, 3, 128):
         got_o, got_l, _ = run_decode(q, k8, v8, sl, n_splits=S, **sc)
         assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 q={q_dtype} G={group} S={S}")
+
+
+@fp8_only
+@pytest.mark.parametrize("S", [10, 11])
+def test_fp8_two_splits_per_cta(S):
+    """More fp8 CTAs than SMs (B x Hkv x S > SMs), so each CTA serves two
+    splits with its two halves of threads and shared memory; with an odd S
+    the second half of each (sequence, KV head)'s last CTA has no split.
+    Ragged lengths with NaN past them; every row against the oracle."""
+    B, Hkv, G, D, T = 2, 8, 4, 128, 3000
+    assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
+    q = fd_inputs.randn((B, Hkv * G, D), "bf16", 1840 + S, device=DEV)
+    k8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1850 + S, device=DEV, gain=GAIN_K)
+    v8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1860 + S, device=DEV, gain=GAIN_V)
+    lens = [3000, 1777]
+    _nan_past_lengths_fp8(k8, lens)
+    _nan_past_lengths_fp8(v8, lens)
+    sl = np.array(lens, dtype=np.int32)
+    sc = dict(k_scale=1 / GAIN_K, v_scale=1 / GAIN_V)
+    ref_o, ref_l = oracle_all(q, k8, v8, sl, "bf16", Hkv, kv_dtype="e4m3", **sc)
+    got_o, got_l, _ = run_decode(q, k8, v8, sl, n_splits=S, **sc)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 two splits per CTA S={S}")
 
 
 @fp8_only
