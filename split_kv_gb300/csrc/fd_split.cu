@@ -148,10 +148,15 @@ constexpr int kOffP = kOffBars + 128;                             // [warps][16 
 constexpr int kOffAlpha = kOffP + kConsumerWarps * 16 * 8 * 4;    // [warps][8] f32
 constexpr int kOffFlag = kOffAlpha + kConsumerWarps * 8 * 4;      // abort flag
 constexpr int kSmemUsed = kOffFlag + 16;
-// end-of-split merge area (reuses stage memory once every stage is consumed)
+// end-of-split merge area (reuses stage memory once every stage is consumed):
+// a row of kAccStride floats per (warp, column), dims d at d + skew * (d / 32)
+// (skew 2 for the tensor-core consumers, 0 for the CUDA-core one), so that the
+// warps' fragment stores meet distinct banks (rows of 128 put the lanes of a
+// store on 4-8 banks) while the merge still reads each row contiguously
 constexpr int kCols = 16;                                         // (query, head) columns per CTA
-constexpr int kOffWAcc = 0;                                       // [warps][16][128] f32
-constexpr int kOffWM = kConsumerWarps * kCols * kHeadDim * 4;     // [warps][16]
+constexpr int kAccStride = 164;                                   // 128 dims + 6 of skew, = 4 mod 32
+constexpr int kOffWAcc = 0;                                       // [warps][16][kAccStride] f32
+constexpr int kOffWM = kConsumerWarps * kCols * kAccStride * 4;   // [warps][16]
 constexpr int kOffWL = kOffWM + kConsumerWarps * kCols * 4;       // [warps][16]
 static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
 
@@ -201,8 +206,9 @@ struct Geo {
     static constexpr int kThreads = (kWarps + (kUmma ? 2 : 1)) * 32;
     static constexpr int kEmptyArrivals = kUmma ? 1 : kWarps;  // tcgen05: the MMA commit
     // end-of-split merge area in stage memory: acc [warps][16][128], m, l [warps][16]
-    static constexpr int kOffWM = kWarps * kCols * kHeadDim * 4;
+    static constexpr int kOffWM = kWarps * kCols * kAccStride * 4;
     static constexpr int kOffWL = kOffWM + kWarps * kCols * 4;
+    static constexpr int kAccSkew = KIND >= 11 && KIND <= 18 ? 0 : 2;   // see the merge area above
     static_assert(2 * kRing * 8 <= 128, "barriers must fit");
     static_assert(kOffWL + kWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
     static_assert(kOwnMap || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
@@ -459,8 +465,8 @@ __device__ __forceinline__ bool consume_simt(const SplitCtx& c, int cw, int lane
         wl[cw * kCols + g_lane] = l_run;
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-        *reinterpret_cast<float4*>(wacc + (cw * kCols + g) * kHeadDim + 4 * lane) =
+    for (int g = 0; g < G; ++g)   // (no skew: whole rows of float4s)
+        *reinterpret_cast<float4*>(wacc + (cw * kCols + g) * kAccStride + 4 * lane) =
             make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
     return true;
 }
@@ -819,9 +825,10 @@ __device__ __forceinline__ bool consume_tc(const SplitCtx& c, int cw, int lane) 
                 wl[cw * kCols + col] = l[j][e];
             }
 #pragma unroll
-            for (int mb = 0; mb < 8; ++mb) {
-                wacc[(cw * kCols + col) * kHeadDim + 16 * mb + gid] = acc[mb][j][e];
-                wacc[(cw * kCols + col) * kHeadDim + 16 * mb + gid + 8] = acc[mb][j][e + 2];
+            for (int mb = 0; mb < 8; ++mb) {   // dims 16 mb + gid (+8): skew 2 * (mb / 2)
+                float* row = wacc + (cw * kCols + col) * kAccStride + 16 * mb + 2 * (mb >> 1);
+                row[gid] = acc[mb][j][e];
+                row[gid + 8] = acc[mb][j][e + 2];
             }
         }
     return true;
@@ -1051,9 +1058,9 @@ __device__ __forceinline__ bool consume_f8(const SplitCtx& c, int cw, int lane) 
                 wl[cw * kCols + col] = l[j][e];
             }
 #pragma unroll
-            for (int mb = 0; mb < 8; ++mb)
-                *reinterpret_cast<float2*>(wacc + (cw * kCols + col) * kHeadDim + 16 * gid + 2 * mb) =
-                    make_float2(acc[mb][j][e], acc[mb][j][e + 2]);
+            for (int mb = 0; mb < 8; ++mb)   // dims 16 gid + 2 mb (+1): skew 2 * (gid / 2)
+                *reinterpret_cast<float2*>(wacc + (cw * kCols + col) * kAccStride + 16 * gid + 2 * (gid >> 1) +
+                                           2 * mb) = make_float2(acc[mb][j][e], acc[mb][j][e + 2]);
         }
     return true;
 }
@@ -1266,7 +1273,7 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads * HALVES, HALVES == 1 ? 2 
             for (int w = 0; w < kWarps; ++w) {
                 const float mw = wm[w * kCols + col];
                 const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                u = fmaf(e, wacc[(w * kCols + col) * kHeadDim + d], u);
+                u = fmaf(e, wacc[(w * kCols + col) * kAccStride + d + Gm::kAccSkew * (d >> 5)], u);
                 l = fmaf(e, wl[w * kCols + col], l);
             }
             m_out = M * kLn2;
