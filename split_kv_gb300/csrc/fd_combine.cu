@@ -27,11 +27,12 @@ constexpr unsigned kFullMask = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;
 constexpr int kWarps = kHeadDim / 32;   // 4
-constexpr int kPre = 8;                 // splits per thread loaded up front (S <= 32: all)
+constexpr int kPre = 9;                 // splits per thread loaded up front (S <= 36: all, so the
+                                        // planner's frequent 33 and 34 take one round trip)
 
 // One CTA (4 warps) per row.  Thread (w, lane) accumulates dims 4*lane..+3
 // over splits i = w, w+4, ..., so the row's S x 128 partial outputs are all
-// in flight at once (up to 32 splits together with m and l); the four warp
+// in flight at once (up to 36 splits together with m and l); the four warp
 // partials are added in a fixed order.
 __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParams p) {
     __shared__ float s_m[kMaxSplits], s_w[kMaxSplits], s_l[kMaxSplits];
@@ -128,10 +129,11 @@ __global__ void __launch_bounds__(kHeadDim) fd_combine_kernel(const CombineParam
 // slower per call at 1024-4096 rows).  Lane l
 // holds dims 4l .. 4l + 3 and the m, l of splits l, l + 32, ...; the partial
 // outputs of the first kPreRows splits are requested together with m and l
-// (one round trip to memory up to 16 splits), the rest kPre at a time, and
+// (one round trip to memory up to 16 splits), the rest kRestRows at a time, and
 // they are added in split order.
 constexpr int kRowsPerCta = 16;
 constexpr int kPreRows = 16;
+constexpr int kRestRows = 8;
 
 __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const CombineParams p) {
     grid_dependency_trigger();
@@ -183,13 +185,13 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) fd_combine_rows_kernel(const
             a.w = fmaf(wt, pre[k].w, a.w);
         }
     }
-    for (int i0 = kPreRows; i0 < S; i0 += kPre) {
-        float4 u[kPre];
+    for (int i0 = kPreRows; i0 < S; i0 += kRestRows) {
+        float4 u[kRestRows];
 #pragma unroll
-        for (int k = 0; k < kPre; ++k)
+        for (int k = 0; k < kRestRows; ++k)
             u[k] = i0 + k < S ? urow[(i0 + k) * kStride] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < kPre; ++k) {
+        for (int k = 0; k < kRestRows; ++k) {
             const float wt = weight(i0 + k);
             if (i0 + k < S) {
                 a.x = fmaf(wt, u[k].x, a.x);
