@@ -122,6 +122,14 @@ __device__ __forceinline__ int ld_relaxed_s32(const int32_t* ptr) {
     return v;
 }
 
+// One 32-byte vector store (the address 32-byte aligned): whole L2 sectors.
+__device__ __forceinline__ void st_global_v8(float* p, float a0, float a1, float a2, float a3, float a4, float a5,
+                                             float a6, float a7) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2),
+                 "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+                 : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

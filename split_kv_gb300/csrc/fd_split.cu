@@ -1926,11 +1926,14 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads, 1)
                             }
                         }
                         if (!p.direct) {
-                            float4* dst = reinterpret_cast<float4*>(p.ws_u + (my_row * S + ci.split) * kHeadDim + 64 * h);
+                            // 32-byte stores: each writes whole sectors of the row's 256 bytes
+                            float* dst = p.ws_u + (my_row * S + ci.split) * kHeadDim + 64 * h;
 #pragma unroll
-                            for (int x = 0; x < 16; ++x)
-                                dst[x] = make_float4(o[4 * x] * p.v_scale, o[4 * x + 1] * p.v_scale,
-                                                     o[4 * x + 2] * p.v_scale, o[4 * x + 3] * p.v_scale);
+                            for (int x = 0; x < 8; ++x)
+                                st_global_v8(dst + 8 * x, o[8 * x] * p.v_scale, o[8 * x + 1] * p.v_scale,
+                                             o[8 * x + 2] * p.v_scale, o[8 * x + 3] * p.v_scale,
+                                             o[8 * x + 4] * p.v_scale, o[8 * x + 5] * p.v_scale,
+                                             o[8 * x + 6] * p.v_scale, o[8 * x + 7] * p.v_scale);
                         } else {   // out carries only its element alignment: scalar stores
                             const int64_t oi = my_row * kHeadDim + 64 * h;
 #pragma unroll
