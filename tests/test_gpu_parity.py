@@ -651,6 +651,34 @@ def test_combine_of_many_rows(out_dtype):
         assert np.all(got_o.reshape(B, -1)[1] == 0.0) and np.all(np.isneginf(got_l.reshape(B, -1)[1]))
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_combine_of_many_rows_unaligned_output(out_dtype):
+    """out carries only its element alignment: the many-rows combine writes
+    an output one element past an aligned address correctly, and the element
+    before it stays untouched."""
+    B, Hkv, G, ql, D, T = 8, 2, 16, 4, 128, 700
+    Hq = Hkv * G
+    rows = B * ql * Hq
+    q = fd_inputs.randn((B, ql, Hq, D), "bf16", 1690, device=DEV)
+    k, v = _cache(B, Hkv, T, D, "bf16", 1691)
+    sl_h = np.array([700, 0, 5, 350, 699, 64, 1, 700], dtype=np.int32)
+    ref_o, ref_l = oracle_all(q, k, v, sl_h, "bf16", Hkv)
+    ref_o = torch.from_numpy(ref_o).to(out_dtype).double().numpy()
+    S = 5
+    desc = fd.make_desc(q, k, v, max_seqlen=int(sl_h.max()), n_splits=S, out_dtype=out_dtype)
+    ws = torch.empty(fd.fd_workspace_size(desc, S), dtype=torch.uint8, device=DEV)
+    backing = torch.full((rows * D + 1,), float("nan"), dtype=out_dtype, device=DEV)
+    out = backing[1:]
+    assert out.data_ptr() % 16 != 0
+    lse = torch.empty(rows, dtype=torch.float32, device=DEV)
+    fd.check(fd.fd_decode(desc, q, k, v, torch.from_numpy(sl_h).to(DEV), None, out, lse, ws), "fd_decode")
+    torch.cuda.synchronize()
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    assert torch.isnan(backing[0]).item()
+    assert_parity(out.double().cpu().numpy().reshape(rows, D), lse.double().cpu().numpy(), ref_o, ref_l,
+                  f"unaligned out {out_dtype}")
+
+
 def test_query_block_wide_paged():
     """A paged 128-column block (G = 16, q_len = 8) on the tcgen05 path."""
     B, Hkv, G, D, ps, ql = 2, 2, 16, 128, 64, 8
