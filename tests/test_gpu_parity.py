@@ -790,6 +790,29 @@ def test_fp8_two_splits_per_cta(S):
 
 @fp8_only
 @pytest.mark.parametrize("ps", [16, 64])
+def test_fp8_paged_two_splits_per_cta(ps):
+    """An fp8 pool through a shuffled block table with more CTAs than SMs
+    (2 x 8 heads x 13 splits), so each CTA serves two splits, the second
+    half of each (sequence, head)'s last CTA idle."""
+    B, Hkv, G, D, S = 2, 8, 4, 128, 13
+    assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
+    lens = [2600, 1333]
+    max_pages = -(-max(lens) // ps)
+    n_pages = B * max_pages + 5
+    pk = fd_inputs.randn_fp8((n_pages, Hkv, ps, D), 1960 + ps, device=DEV, gain=GAIN_K)
+    pv = fd_inputs.randn_fp8((n_pages, Hkv, ps, D), 1961 + ps, device=DEV, gain=GAIN_V)
+    bt = fd_inputs.page_permutation(1962 + ps, n_pages)[:B * max_pages].reshape(B, max_pages).copy()
+    q = fd_inputs.randn((B, Hkv * G, D), "bf16", 1963 + ps, device=DEV)
+    sl = np.array(lens, dtype=np.int32)
+    sc = dict(k_scale=1 / GAIN_K, v_scale=1 / GAIN_V)
+    ref_o, ref_l = oracle_all(q, pk, pv, sl, "bf16", Hkv, page_size=ps, block_table=bt,
+                              kv_dtype="e4m3", **sc)
+    got_o, got_l, _ = run_decode(q, pk, pv, sl, page_size=ps, block_table=bt, n_splits=S, **sc)
+    assert_parity(got_o, got_l, ref_o, ref_l, f"fp8 paged two splits per CTA ps={ps}")
+
+
+@fp8_only
+@pytest.mark.parametrize("ps", [16, 64])
 def test_fp8_paged_and_query_block(ps):
     """An fp8 pool read through a shuffled block table, with a 4-position
     query block of a G = 4 group (16 columns: two MMA N blocks)."""
