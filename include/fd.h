@@ -43,11 +43,12 @@
  *    already in the cache, in order); a position that sees no key gets
  *    out = 0 and lse = -inf.  Every (position, head) of a KV head's group is
  *    one column of the CTA's tensor-core tile.  Up to 16 columns: one CTA per
- *    split on warp MMAs.  17-128 columns with a 16-bit cache (and no
- *    FD_FLAG_CUDA_CORES): one CTA per split on tcgen05 MMAs, all columns as
- *    the M rows of one 128-row tile (launched as a persistent grid of at most
- *    one CTA per SM that serves the splits in turn).  Otherwise ceil(G*q_len/16) CTAs per
- *    split, each reading the split's K/V once.
+ *    split on warp MMAs (an fp8 cache with up to 8 columns: a CTA serves two
+ *    splits once splits outnumber SMs).  17-128 columns with a 16-bit cache
+ *    (and no FD_FLAG_CUDA_CORES): one CTA per split on tcgen05 MMAs, all
+ *    columns as the M rows of one 128-row tile (launched as a persistent grid
+ *    of at most one CTA per SM that serves the splits in turn).  Otherwise
+ *    ceil(G*q_len/16) CTAs per split, each reading the split's K/V once.
  *  - Supported shapes: head_dim 128; G = n_q_heads / n_kv_heads and q_len
  *    with G*q_len <= 256 and q_len <= 16 (with FD_FLAG_CUDA_CORES: G in
  *    {1, 2, 4, 8}, q_len = 1 and a 16-bit cache); kv_dtype FD_F16, FD_BF16 or

@@ -1,6 +1,7 @@
 // fd_split.cu -- the split kernel of split-KV decode attention on sm_103a.
 //
-// One CTA per (KV split, KV head, sequence).  It streams the split's K/V
+// One CTA per (KV split, KV head, sequence) (the fp8 kernel with up to 8
+// columns: two per CTA once splits outnumber SMs).  It streams the split's K/V
 // rows once, for all G query heads of the KV head's group, and leaves the
 // group's unnormalised partial states (u, m, l) in the workspace:
 //   m = max_j s_j,  l = sum_j exp(s_j - m),  u = sum_j exp(s_j - m) v_j
@@ -26,10 +27,13 @@
 //    consume_f8 builds the same MMAs' fragments from e4m3 bytes in registers;
 //    consume_simt (FD_FLAG_CUDA_CORES) uses FP32 FMAs, a half-warp per K row.
 //  - Query blocks of 17-128 columns on a 16-bit cache run instead on 5th-
-//    generation tensor cores (fd_split_umma_kernel): a persistent grid of one
-//    CTA per SM serves the splits in turn, each holding every column as the M
-//    rows of tcgen05 MMAs with S and O accumulated in tensor memory, fed by the
-//    same TMA stages laid out in pairs.
+//    generation tensor cores (fd_split_umma_kernel): a persistent grid of at
+//    most one CTA per SM serves the splits in turn, each holding every column
+//    as the M rows of tcgen05 MMAs with S and O accumulated in tensor memory,
+//    fed by the same TMA stages laid out in pairs.
+//  - Before its launch wait, a CTA of the warp-MMA kernels prefetches the
+//    first tokens of its split into L2, so its first stages overlap the tail
+//    of the kernel before it in the stream.
 //  - Scores are kept in base 2: t = (q.k) * log2(e)/sqrt(D), p = 2^(t - m).
 //    The workspace m is converted back to natural units of s.
 //  - Every mbarrier wait is bounded (2 s of wall time); on timeout the kernel
@@ -168,7 +172,8 @@ static_assert(kOffWL + kConsumerWarps * kCols * 4 <= kOffBars, "merge area must 
 // per stage, read by the consumers straight into registers; with at most 8
 // columns per CTA (KIND 21) six consumer warps take 96-token stages, 4 deep,
 // otherwise (KIND 22) four take 64-token stages, 6 deep.  Either way the ring
-// holds 96 KB, and two CTAs fit on an SM.
+// holds 96 KB, and two CTAs (or the two halves of a KIND 21 CTA that serves
+// two splits) fit on an SM.
 template <int KIND>
 struct Geo {
     static constexpr bool kUmma = KIND == 31 || KIND == 32;    // tcgen05 consumers, see below
