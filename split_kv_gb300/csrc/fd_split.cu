@@ -213,9 +213,14 @@ struct Geo {
     // end-of-split merge area in stage memory: acc [warps][16][128], m, l [warps][16]
     static constexpr int kOffWM = kWarps * kCols * kAccStride * 4;
     static constexpr int kOffWL = kOffWM + kWarps * kCols * 4;
+    // per column, from the merge's first phase: state row, warp weights, m, l
+    static constexpr int kOffCRow = (kOffWL + kWarps * kCols * 4 + 7) / 8 * 8;   // int64 [kCols]
+    static constexpr int kOffCW = kOffCRow + kCols * 8;                          // [kCols][kWarps]
+    static constexpr int kOffCM = kOffCW + kCols * kWarps * 4;                   // [kCols]
+    static constexpr int kOffCL = kOffCM + kCols * 4;                            // [kCols]
     static constexpr int kAccSkew = KIND >= 11 && KIND <= 18 ? 0 : 2;   // see the merge area above
     static_assert(2 * kRing * 8 <= 128, "barriers must fit");
-    static_assert(kOffWL + kWarps * kCols * 4 <= kOffBars, "merge area must fit in the stages");
+    static_assert(kOffCL + kCols * 4 <= kOffBars, "merge area must fit in the stages");
     static_assert(kOwnMap || (kSub == fdk::kSub && kStageBytes == fdk::kStageBytes &&
                               kOffBars == fdk::kOffBars), "16-bit variants use the map above");
 };
@@ -1260,33 +1265,49 @@ __global__ void __launch_bounds__(Geo<KIND>::kThreads * HALVES, HALVES == 1 ? 2 
 
     if (!Consumer<T, KIND>::run(c, warp, lane)) return;
     named_sync(c.bar_id, kWarps * 32);
-    if (tid >= kHeadDim) return;   // one thread per dim below
 
-    // ---- merge the consumer warps' states of each column and write the split's state
+    // ---- merge the consumer warps' states of each column and write the split's
+    // state, in two phases so that the columns' dependent chains run side by
+    // side: one thread per column takes the max, the warps' weights and l
+    // (and the state row), then one thread per dim sums its u over the warps
     const float* wacc = reinterpret_cast<const float*>(smem);
     const float* wm = reinterpret_cast<const float*>(smem + Gm::kOffWM);
     const float* wl = reinterpret_cast<const float*>(smem + Gm::kOffWL);
-    const int d = tid;   // 0 .. 127
+    int64_t* crow = reinterpret_cast<int64_t*>(smem + Gm::kOffCRow);
+    float* cw = reinterpret_cast<float*>(smem + Gm::kOffCW);
+    float* cm = reinterpret_cast<float*>(smem + Gm::kOffCM);
+    float* cl = reinterpret_cast<float*>(smem + Gm::kOffCL);
     const int ncols = min(kCols, p.cols - c.cb * kCols);
-    for (int col = 0; col < ncols; ++col) {
+    if (tid < ncols) {
+        const int col = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kCols + col]);
-        float u = 0.f, l = 0.f, m_out = -INFINITY;
-        if (M != -INFINITY) {
+        float l = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = wm[w * kCols + col];
-                const float e = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                u = fmaf(e, wacc[(w * kCols + col) * kAccStride + d + Gm::kAccSkew * (d >> 5)], u);
-                l = fmaf(e, wl[w * kCols + col], l);
-            }
-            m_out = M * kLn2;
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = wm[w * kCols + col];
+            const float e = (M == -INFINITY || mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            cw[col * kWarps + w] = e;
+            l = fmaf(e, wl[w * kCols + col], l);
         }
+        cm[col] = M == -INFINITY ? -INFINITY : M * kLn2;
+        cl[col] = l;
         const int n = c.cb * kCols + col;
         const int i = n / p.group, g = n % p.group;
-        const int64_t row = (static_cast<int64_t>(c.b) * p.q_len + i) * p.n_q_heads +
-                            c.kvh * p.group + g;
+        crow[col] = (static_cast<int64_t>(c.b) * p.q_len + i) * p.n_q_heads + c.kvh * p.group + g;
+    }
+    named_sync(c.bar_id, kWarps * 32);
+    if (tid >= kHeadDim) return;   // one thread per dim below
+    const int d = tid;   // 0 .. 127
+    const int dd = d + Gm::kAccSkew * (d >> 5);
+#pragma unroll 1
+    for (int col = 0; col < ncols; ++col) {
+        float u = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) u = fmaf(cw[col * kWarps + w], wacc[(w * kCols + col) * kAccStride + dd], u);
+        const float m_out = cm[col], l = cl[col];
+        const int64_t row = crow[col];
         const int64_t idx = row * S + c.split;
         const float us = u * p.v_scale;   // values are v_scale x the stored ones
         if (p.direct) {
