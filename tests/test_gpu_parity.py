@@ -575,6 +575,45 @@ def test_fd_decode_replays_from_a_cuda_graph():
     assert fd.fd_device_status(clear=True) == fd.FD_OK
 
 
+@pytest.mark.parametrize("kind", ["f16", "e4m3"])
+def test_lengths_written_by_the_kernel_before(kind):
+    """The split kernels prefetch the first tokens of their split into L2
+    ahead of their launch wait, from a length read without waiting.  Here a
+    kernel just before each call in the stream writes new lengths (longer,
+    shorter, empty), with no synchronisation in between; every result is
+    checked against the oracle.  The fp8 case runs the two-split CTA."""
+    if kind == "e4m3" and not FP8:
+        pytest.skip("torch without float8_e4m3fn")
+    B, Hq, Hkv, D, T, S = 2, 32, 8, 128, 4096, 10
+    q = fd_inputs.randn((B, Hq, D), "f16", 1311, device=DEV)
+    sc = {}
+    if kind == "e4m3":
+        k = fd_inputs.randn_fp8((B, Hkv, T, D), 1312, device=DEV, gain=GAIN_K)
+        v = fd_inputs.randn_fp8((B, Hkv, T, D), 1313, device=DEV, gain=GAIN_V)
+        sc = dict(k_scale=1 / GAIN_K, v_scale=1 / GAIN_V)
+    else:
+        k, v = _cache(B, Hkv, T, D, "f16", 1312)
+    seqlens = torch.zeros(B, dtype=torch.int32, device=DEV)
+    desc = fd.make_desc(q, k, v, max_seqlen=T, n_splits=S, **sc)
+    ws = torch.empty(fd.fd_workspace_size(desc, S), dtype=torch.uint8, device=DEV)
+    outs = []
+    all_lens = ([4096, 100], [37, 4000], [2048, 2049], [0, 4096], [4096, 4096])
+    for lens in all_lens:
+        src = torch.tensor(lens, dtype=torch.int32, device=DEV)
+        torch.add(src, 0, out=seqlens)            # a kernel writes the lengths
+        out = torch.empty(B, Hq, D, dtype=torch.float32, device=DEV)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=DEV)
+        fd.check(fd.fd_decode(desc, q, k, v, seqlens, None, out, lse, ws), "fd_decode")
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    assert fd.fd_device_status(clear=True) == fd.FD_OK
+    for lens, (out, lse) in zip(all_lens, outs):
+        ref_o, ref_l = oracle_all(q, k, v, np.array(lens, dtype=np.int32), "f16", Hkv,
+                                  kv_dtype="e4m3" if kind == "e4m3" else None, **sc)
+        assert_parity(out.cpu().double().numpy().reshape(B * Hq, D), lse.cpu().double().numpy().reshape(-1),
+                      ref_o, ref_l, f"lengths {lens} ({kind})")
+
+
 # ---------------------------------------------------------------- query blocks, any group
 @pytest.mark.parametrize("q_len", [2, 4, 8])
 @pytest.mark.parametrize("group", [1, 3, 4, 8])
