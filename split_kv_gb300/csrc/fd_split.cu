@@ -2094,9 +2094,14 @@ static cudaError_t launch_split_t(const CUtensorMap& tmK, const CUtensorMap& tmV
     using Gm = Geo<KIND>;
     const int blocks = p.n_splits * p.col_blocks;
     // fp8, up to 8 columns: its consumers do not keep up with HBM on an SM of
-    // their own, so once splits outnumber SMs every CTA takes two
+    // their own, so once splits outnumber SMs every CTA takes two -- while one
+    // wave holds those CTAs (a CTA of two takes a whole SM, and an odd split
+    // count leaves a half idle per (sequence, KV head); beyond one wave the
+    // CTAs of one, two to an SM, quantise better)
     if constexpr (KIND == 21) {
-        if (static_cast<int64_t>(blocks) * n_kv_heads * batch > fd_num_sms(-1)) {
+        const int sms = fd_num_sms(-1);
+        const int64_t heads = static_cast<int64_t>(n_kv_heads) * batch;
+        if (blocks * heads > sms && ((blocks + 1) / 2) * heads <= sms) {
             auto kern = fd_split_kernel<T, KIND, 2>;
             const size_t smem = 2 * Gm::kSmemHalf + 1024;
             static std::atomic<unsigned long long> configured_ctx2{0};

@@ -516,7 +516,8 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(kind):
     S = 20 if kind == "e4m3_two_per_cta" else 1
     B, Hkv, D, T = 1, 8 if G == 1 else 2, 128, 300 * S
     if S > 1:
-        assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
+        sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+        assert sms < B * Hkv * S and -(-S // 2) * B * Hkv <= sms   # the two-split CTA's range
     Hq = Hkv * G
     q = fd_inputs.randn((B, ql, Hq, D) if ql > 1 else (B, Hq, D), dt, 1201, device=DEV)
     sc = {}
@@ -808,12 +809,14 @@ def test_fp8_cache(q_dtype, group):
 @fp8_only
 @pytest.mark.parametrize("S", [10, 11])
 def test_fp8_two_splits_per_cta(S):
-    """More fp8 CTAs than SMs (B x Hkv x S > SMs), so each CTA serves two
-    splits with its two halves of threads and shared memory; with an odd S
-    the second half of each (sequence, KV head)'s last CTA has no split.
+    """More fp8 splits than SMs, with the CTAs of two splits (ceil(S / 2) per
+    sequence and KV head) in one wave, so each CTA serves two splits with its
+    two halves of threads and shared memory; with an odd S the second half
+    of each (sequence, KV head)'s last CTA has no split.
     Ragged lengths with NaN past them; every row against the oracle."""
     B, Hkv, G, D, T = 2, 8, 4, 128, 3000
-    assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert sms < B * Hkv * S and -(-S // 2) * B * Hkv <= sms   # the two-split CTA's range
     q = fd_inputs.randn((B, Hkv * G, D), "bf16", 1840 + S, device=DEV)
     k8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1850 + S, device=DEV, gain=GAIN_K)
     v8 = fd_inputs.randn_fp8((B, Hkv, T, D), 1860 + S, device=DEV, gain=GAIN_V)
@@ -834,7 +837,8 @@ def test_fp8_paged_two_splits_per_cta(ps):
     (2 x 8 heads x 13 splits), so each CTA serves two splits, the second
     half of each (sequence, head)'s last CTA idle."""
     B, Hkv, G, D, S = 2, 8, 4, 128, 13
-    assert B * Hkv * S > torch.cuda.get_device_properties(DEV).multi_processor_count
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert sms < B * Hkv * S and -(-S // 2) * B * Hkv <= sms   # the two-split CTA's range
     lens = [2600, 1333]
     max_pages = -(-max(lens) // ps)
     n_pages = B * max_pages + 5
